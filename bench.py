@@ -1,0 +1,426 @@
+#!/usr/bin/env python3
+"""Benchmark of split-KV decode attention on one GB300 (or N, one process each).
+
+One step = one ``fd_decode`` call (plan, split, merge: a single kernel launch)
+over the batch-1 128k-context GQA workload (B=1, Hq=32, Hkv=8, D=128,
+T=131072, bf16 K/V, fp32 q/out), inputs resident in HBM.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {fdecode,reference}] [--workload 1..5]
+
+``--impl reference`` times the float64 CPU oracle (the only reference this
+method has) on the host cores, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/step; KV-read HBM GB/s as % of GB300 peak (1 GPU)"
+DEFAULT_WORKLOAD = 3
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["fdecode", "reference"], default="fdecode")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "split_kv_decode_fd_gb300", "csrc", "*"))):
+        if p.endswith((".cu", ".cuh", ".h")):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:12]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel sources."""
+    for p in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        txt = open(p).read()
+        if f"workload: {workload_name}" not in txt:
+            continue
+        vals = {}
+        for line in txt.splitlines():
+            if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha")):
+                k, v = line.split(":", 1)
+                vals[k.strip("-* `")] = v.strip(" `")
+        if vals.get("source_sha") == source_hash() and "traffic_bytes_per_launch" in vals:
+            try:
+                return int(float(vals["traffic_bytes_per_launch"]))
+            except ValueError:
+                return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        inside = [ln for t, ln in self.lines if t0 <= t <= t1] or [ln for _, ln in self.lines[-1:]]
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in inside:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def workload_bytes(case) -> int:
+    """Algorithmic bytes of one step: valid K+V rows, q in, out written (as the metric counts them)."""
+    s = case.spec
+    return case.kv_bytes() + s.B * s.Hq * s.D * 4 * 2
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return int(os.environ.get("OMP_NUM_THREADS", cpu_cores()))
+
+
+class OracleSampler:
+    """Host-side copy of a workload for timing the float64 oracle on bounded samples."""
+
+    def __init__(self, case):
+        import numpy as np
+        self.np = np
+        self.case = case
+        s = case.spec
+        self.g = s.Hq // s.Hkv
+        self.q = case.q.detach().cpu().numpy().astype(np.float64)
+        self.lens = case.lengths
+        self.k = case.k.detach().cpu()
+        self.v = case.v.detach().cpu()
+        self.table = None if case.block_table is None else case.block_table.cpu().numpy()
+        self.es = case.k.element_size()
+
+    def group(self, b, kvh, n_tok=None):
+        """Oracle on the first n_tok keys of (b, kv head) for its g query heads: (seconds, kv bytes)."""
+        import oracle
+        np, s = self.np, self.case.spec
+        L = self.lens[b] if n_tok is None else min(n_tok, self.lens[b])
+        qb = self.q[b:b + 1, kvh * self.g:(kvh + 1) * self.g]
+        if self.table is None:
+            kb = self.k[b:b + 1, kvh:kvh + 1, :L].float().numpy()
+            vb = self.v[b:b + 1, kvh:kvh + 1, :L].float().numpy()
+            t0 = time.perf_counter()
+            oracle.decode(qb, kb, vb, s.scale, seq_lens=[L], max_seq_len=L)
+        else:
+            npg = -(-L // s.page_size)
+            pages = self.table[b, :npg]
+            kb = self.k[pages][:, kvh:kvh + 1].float().numpy()
+            vb = self.v[pages][:, kvh:kvh + 1].float().numpy()
+            t0 = time.perf_counter()
+            oracle.decode(qb, kb, vb, s.scale, seq_lens=[L], block_table=np.arange(npg)[None],
+                          page_size=s.page_size)
+        return time.perf_counter() - t0, L * s.D * 2 * self.es
+
+    def whole_groups(self, seconds):
+        """Whole (b, kv head) groups in order until `seconds` of oracle time: (GB/s, note, seconds)."""
+        s = self.case.spec
+        done, el, n = 0, 0.0, 0
+        for b in range(s.B):
+            for kvh in range(s.Hkv):
+                if self.lens[b] == 0:
+                    continue
+                t, nb = self.group(b, kvh)
+                el, done, n = el + t, done + nb, n + 1
+                if el >= seconds:
+                    break
+            if el >= seconds:
+                break
+        note = (f"{n} of {s.B * s.Hkv} whole (batch, kv-head) groups, {self.g} query heads each; "
+                "float64 NumPy oracle")
+        return done / el / 1e9, note, el
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    from workloads import CONFIGS, make_case
+    spec = CONFIGS[args.workload]
+    smp = OracleSampler(make_case(spec, "cpu"))
+    b0 = next(b for b, L in enumerate(smp.lens) if L > 0)
+    # each step: the oracle on the first n_tok keys of one (b, kv-head) group, sized so
+    # that warm-up plus timed steps take about two minutes of host time
+    budget = max(0.01, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    t_probe, _ = smp.group(b0, 0, 4096)
+    n_tok = int(min(smp.lens[b0], max(128, 4096 * budget / max(t_probe, 1e-6))))
+    for _ in range(args.warmup):
+        smp.group(b0, 0, n_tok)
+    secs, nbytes = [], 0
+    for i in range(args.steps):
+        t, nb = smp.group(b0, i % spec.Hkv, n_tok)
+        secs.append(t)
+        nbytes += nb
+    value = nbytes / sum(secs) / 1e9
+    cores = blas_threads()
+    note = (f"per step: first {n_tok} keys of one (batch, kv-head) group ({smp.g} query heads), "
+            "float64 NumPy oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": spec.name, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv,
+                                        "D": spec.D, "T": spec.T_cap, "kv_dtype": spec.kv_dtype},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": note},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_fdecode(args):
+    world, rank, local = dist_env()
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (libfdecode has no CPU path)")
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    import split_kv_decode_fd_gb300 as fd
+    from workloads import CONFIGS, make_case
+    fd.load_library()
+
+    spec = CONFIGS[args.workload]
+    case = make_case(spec, device)
+    step_bytes = workload_bytes(case)
+    kv_bytes = case.kv_bytes()
+    out = torch.empty((spec.B, spec.Hq, spec.D), dtype=torch.float32, device=device)
+    lse = torch.empty((spec.B, spec.Hq), dtype=torch.float32, device=device)
+    ws = fd.Workspace()
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        fd.decode(case.q, case.k, case.v, seq_lens=case.seq_lens, max_seq_len=case.max_seq_len,
+                  block_table=case.block_table, scale=spec.scale, n_splits=spec.n_splits, out=out, lse=lse,
+                  workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if fd.workspace_status(ws) != 0:
+        raise SystemExit("kernel reported an error during warm-up")
+
+    # ---- timed region: K steps, per-launch events, clocks sampled meanwhile
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device.index or 0)
+    sampler.start()
+    time.sleep(0.2)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    barrier(world)
+    clocks = sampler.stop(t0, t1)
+    total_ms = start.elapsed_time(end)
+    launch_us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    total_ms = max_over_ranks(total_ms, world, device)
+    ms_per_step = total_ms / K
+    value = world * step_bytes * K / (total_ms * 1e-3) / 1e9
+    mean_launch_us = statistics.mean(launch_us)
+    achieved = step_bytes / (mean_launch_us * 1e-6) / 1e9
+    peak, peak_src = measured_peak()
+
+    # ---- end to end: host q in, host out/lse back, through fd_decode_host
+    q_host = case.q.cpu().pin_memory()
+    lens_host = None if case.seq_lens is None else case.seq_lens.cpu()
+    out_h = torch.empty((spec.B, spec.Hq, spec.D), dtype=torch.float32, pin_memory=True)
+    lse_h = torch.empty((spec.B, spec.Hq), dtype=torch.float32, pin_memory=True)
+    ws_h = fd.Workspace()
+
+    def e2e_step():
+        fd.decode_host(q_host, case.k, case.v, seq_lens_host=lens_host, max_seq_len=case.max_seq_len,
+                       block_table=case.block_table, scale=spec.scale, n_splits=spec.n_splits, out_host=out_h,
+                       lse_host=lse_h, workspace=ws_h)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    k_e2e = max(10, min(K, 2000))
+    barrier(world)
+    te0 = time.perf_counter()
+    for _ in range(k_e2e):
+        e2e_step()
+    te1 = time.perf_counter()
+    e2e_s = max_over_ranks(te1 - te0, world, device)
+    e2e_value = world * step_bytes * k_e2e / e2e_s / 1e9
+    h2d = q_host.numel() * 4 + (0 if lens_host is None else lens_host.numel() * 4)
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+    # ---- CPU baseline: the oracle on a bounded sample, host cores, rank 0 at N=1
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v, note, el = OracleSampler(case).whole_groups(args.cpu_seconds)
+        cpu = {"value": v, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle", "sample": note,
+               "seconds": round(el, 2)}
+
+    gpd = fd.workspace_status(ws)
+    g = spec.Hq // spec.Hkv
+    gpad = 1
+    while gpad < g and gpad < 8:
+        gpad *= 2
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "us_per_step": ms_per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": spec.name, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "D": spec.D,
+                   "T": spec.T_cap, "kv_dtype": spec.kv_dtype, "q_dtype": "f32", "layout": spec.layout,
+                   "kv_bytes_per_step": kv_bytes, "bytes_per_step": step_bytes,
+                   "l2": f"inputs {kv_bytes / 1e6:.0f} MB > 129 MB L2; no flush",
+                   "plan": "balanced" if spec.n_splits == 0 else f"n_splits={spec.n_splits}",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "kernel": f"fd_split_kernel<D={spec.D},{spec.kv_dtype},G={gpad}> (fused LSE merge)",
+                   "launch_us_p10_p50_p90": [round(x, 2) for x in statistics.quantiles(launch_us, n=10)[0::4]]},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(spec.name),
+                     "peak_source": peak_src, "kernel": "fd_split_kernel", "launches_per_step": 1,
+                     "mean_launch_us": mean_launch_us},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": k_e2e, "api": "fd_decode_host"},
+        "gpu_launches": K,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "kernel_status": gpd,
+        "source_sha": source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_fdecode(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,443 @@
+// fd_api.cu -- the C ABI of libfdecode: argument checks, workspace layout,
+// TMA descriptors, the host-side plan inspector and kernel dispatch.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/fdecode.h"
+#include "fd_internal.h"
+#include "fd_split.cuh"
+
+using namespace fdk;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kHeaderBytes = 256;  // error word + reserved
+// Arrival counters of the fused merge live in a region of fixed size right
+// after the header, whatever the problem shape, so that no call ever writes
+// partials where another shape keeps its counters; every call leaves the
+// counters it used at zero.
+constexpr int64_t kMaxFusedPairs = 65536;
+constexpr size_t kCounterBytes = (size_t)kMaxFusedPairs * 4;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Balanced plan CTA count for the current device (one CTA per SM).
+int sm_count(int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static std::atomic<int> cache[64];
+  if (dev >= 0 && dev < 64) {
+    int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) {
+      *out = c;
+      return 1;
+    }
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  *out = n;
+  return 1;
+}
+
+struct WsLayout {
+  size_t err, counters, o, m, l, q_stage, out_stage, lse_stage, len_stage, total;
+};
+
+// Workspace: [header | counters | o | m | l | host staging (q, out, lse, lens)].
+WsLayout ws_layout(int B, int Hq, int Hkv, int D, int n_splits, int grid) {
+  const Groups gr = make_groups(Hq, Hkv);
+  const size_t pairs = (size_t)B * gr.hv;
+  size_t states;  // number of (slot, head) partial states
+  if (n_splits == 0)
+    states = ((size_t)grid + pairs) * gr.gpad;  // slots <= grid + pairs - 1
+  else
+    states = (size_t)B * Hq * n_splits;
+  WsLayout w;
+  w.err = 0;
+  w.counters = kHeaderBytes;
+  w.o = w.counters + kCounterBytes;
+  w.m = w.o + align_up(states * D * 4);
+  w.l = w.m + align_up(states * 4);
+  w.q_stage = w.l + align_up(states * 4);
+  w.out_stage = w.q_stage + align_up((size_t)B * Hq * D * 4);
+  w.lse_stage = w.out_stage + align_up((size_t)B * Hq * D * 4);
+  w.len_stage = w.lse_stage + align_up((size_t)B * Hq * 4);
+  w.total = w.len_stage + align_up((size_t)B * 4);
+  return w;
+}
+
+fd_status check_shape(int B, int Hq, int Hkv, int D) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FD_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FD_ERR_UNSUPPORTED;
+  const Groups gr = make_groups(Hq, Hkv);
+  if ((int64_t)B * gr.hv > (int64_t)1 << 30) return FD_ERR_UNSUPPORTED;
+  return FD_OK;
+}
+
+fd_status check_kv(const fd_kv_desc* kv, int B, int Hkv, int max_seq_len) {
+  if (!kv || !kv->k || !kv->v) return FD_ERR_INVALID_ARG;
+  if (!aligned16(kv->k) || !aligned16(kv->v)) return FD_ERR_INVALID_ARG;
+  if (kv->dtype != FD_F32 && kv->dtype != FD_BF16) return FD_ERR_UNSUPPORTED;
+  if (max_seq_len < 0) return FD_ERR_INVALID_ARG;
+  const int64_t tiles = (int64_t)B * Hkv * ((max_seq_len + kPlanTile - 1) / kPlanTile);
+  if (tiles >= ((int64_t)1 << 31) / kMaxGroup) return FD_ERR_UNSUPPORTED;
+  if (kv->layout == FD_KV_CONTIGUOUS) {
+    if (kv->capacity < 1 || kv->capacity < max_seq_len) return FD_ERR_INVALID_ARG;
+    if (kv->capacity > ((int64_t)1 << 31) - 1) return FD_ERR_UNSUPPORTED;
+  } else if (kv->layout == FD_KV_PAGED) {
+    if (!kv->block_table || kv->page_size < 16 || kv->page_size % 16 != 0 || kv->num_pages < 1 ||
+        kv->max_pages_per_seq < 1)
+      return FD_ERR_INVALID_ARG;
+    if ((int64_t)kv->max_pages_per_seq * kv->page_size < max_seq_len) return FD_ERR_INVALID_ARG;
+  } else {
+    return FD_ERR_INVALID_ARG;
+  }
+  return FD_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 16-row x 128-byte boxes with the 128-byte swizzle, over the contiguous
+// cache [B*Hkv, T_cap, D] or the page pool [num_pages, Hkv, page_size, D].
+fd_status make_maps(const fd_kv_desc* kv, int B, int Hkv, int D, CUtensorMap* tk, CUtensorMap* tv) {
+  auto encode = encode_fn();
+  if (!encode) return FD_ERR_CUDA;
+  const CUtensorMapDataType dt =
+      kv->dtype == FD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const cuuint64_t es = kv->dtype == FD_BF16 ? 2 : 4;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+  cuuint32_t rank;
+  if (kv->layout == FD_KV_CONTIGUOUS) {
+    rank = 3;
+    dims[0] = (cuuint64_t)D;
+    dims[1] = (cuuint64_t)kv->capacity;
+    dims[2] = (cuuint64_t)B * Hkv;
+    strides[0] = (cuuint64_t)D * es;
+    strides[1] = (cuuint64_t)kv->capacity * D * es;
+    box[0] = (cuuint32_t)(128 / es);
+    box[1] = 16;
+    box[2] = 1;
+  } else {
+    rank = 4;
+    dims[0] = (cuuint64_t)D;
+    dims[1] = (cuuint64_t)kv->page_size;
+    dims[2] = (cuuint64_t)Hkv;
+    dims[3] = (cuuint64_t)kv->num_pages;
+    strides[0] = (cuuint64_t)D * es;
+    strides[1] = (cuuint64_t)kv->page_size * D * es;
+    strides[2] = (cuuint64_t)Hkv * kv->page_size * D * es;
+    box[0] = (cuuint32_t)(128 / es);
+    box[1] = 16;
+    box[2] = 1;
+    box[3] = 1;
+  }
+  const void* ptrs[2] = {kv->k, kv->v};
+  CUtensorMap* maps[2] = {tk, tv};
+  for (int i = 0; i < 2; ++i) {
+    CUresult r = encode(maps[i], dt, rank, const_cast<void*>(ptrs[i]), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return FD_ERR_INVALID_ARG;
+  }
+  return FD_OK;
+}
+
+SplitParams base_params(const float* q, const fd_kv_desc* kv, int B, int Hq, int Hkv,
+                        const int32_t* seq_lens, int max_seq_len, float scale) {
+  SplitParams p;
+  std::memset(&p, 0, sizeof(p));
+  const Groups gr = make_groups(Hq, Hkv);
+  p.q = q;
+  p.seq_lens = seq_lens;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.g = gr.g;
+  p.gpad = gr.gpad;
+  p.nsub = gr.nsub;
+  p.hv = gr.hv;
+  p.max_len = max_seq_len;
+  p.paged = kv->layout == FD_KV_PAGED;
+  p.block_table = kv->block_table;
+  p.page_size = kv->page_size;
+  p.max_pages = kv->max_pages_per_seq;
+  p.num_pages = kv->num_pages;
+  p.qk_scale = (float)((double)scale * 1.4426950408889634);
+  return p;
+}
+
+// Split count used when the balanced plan does not apply (batch above
+// FD_AUTO_MAX_BATCH): about two CTAs per SM over all (b, virtual kv head).
+int fallback_splits(int B, int hv, int max_seq_len, int sms) {
+  const int64_t pairs = (int64_t)B * hv;
+  int64_t n = (2 * (int64_t)sms + pairs - 1) / pairs;
+  const int64_t cap = (max_seq_len + kPlanTile - 1) / kPlanTile;
+  if (n > cap) n = cap;
+  return (int)(n < 1 ? 1 : (n > 65535 ? 65535 : n));
+}
+
+fd_status launch(const fd_kv_desc* kv, int D, const SplitParams& p, dim3 grid, cudaStream_t stream) {
+  CUtensorMap tk, tv;
+  fd_status st = make_maps(kv, p.B, p.Hkv, D, &tk, &tv);
+  if (st != FD_OK) return st;
+  cudaError_t e = kv->dtype == FD_BF16 ? launch_split_bf16(D, p.gpad, tk, tv, p, grid, stream)
+                                       : launch_split_f32(D, p.gpad, tk, tv, p, grid, stream);
+  return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+// Host copy of the per-sequence tile table, for the plan inspector.
+struct HostTiles {
+  const int32_t* pre;
+  const int32_t* ln;
+  FD_HD int32_t prefix(int32_t b) const { return pre[b]; }
+  FD_HD int32_t tiles(int32_t b) const { return pre[b + 1] - pre[b]; }
+  FD_HD int32_t len(int32_t b) const { return ln[b]; }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* fd_status_string(fd_status s) {
+  switch (s) {
+    case FD_OK: return "ok";
+    case FD_ERR_INVALID_ARG: return "invalid argument";
+    case FD_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case FD_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case FD_ERR_BAD_INDEX: return "block-table entry out of range";
+    case FD_ERR_CUDA: return "CUDA error";
+    case FD_ERR_TIMEOUT: return "kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+int32_t fd_version(void) { return 100; }
+
+int32_t fd_split_size(int32_t max_seq_len, int32_t n_splits) {
+  return explicit_split_size(max_seq_len, n_splits);
+}
+
+size_t fd_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t n_splits, int32_t num_sms) {
+  if (check_shape(B, Hq, Hkv, D) != FD_OK || n_splits < 0 || n_splits > 65535) return 0;
+  int grid = num_sms;
+  if (grid <= 0 && !sm_count(&grid)) return 0;
+  const Groups gr = make_groups(Hq, Hkv);
+  if (n_splits == 0 && (B > FD_AUTO_MAX_BATCH || (int64_t)B * gr.hv > kMaxFusedPairs)) {
+    // the fallback split count depends on max_seq_len; size for the largest it can be
+    const size_t a = ws_layout(B, Hq, Hkv, D, fallback_splits(B, gr.hv, 1 << 30, grid), grid).total;
+    return a;
+  }
+  return ws_layout(B, Hq, Hkv, D, n_splits, grid).total;
+}
+
+fd_status fd_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < kHeaderBytes) return FD_ERR_INVALID_ARG;
+  return cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream) == cudaSuccess ? FD_OK
+                                                                                                : FD_ERR_CUDA;
+}
+
+fd_status fd_workspace_status(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < kHeaderBytes) return FD_ERR_INVALID_ARG;
+  unsigned word = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FD_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FD_ERR_CUDA;
+  if (word == 0) return FD_OK;
+  if (cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    return FD_ERR_CUDA;
+  if (word & kErrTimeout) return FD_ERR_TIMEOUT;
+  return FD_ERR_BAD_INDEX;
+}
+
+fd_status fd_decode(const float* q, const fd_kv_desc* kv, float* out, float* lse, int32_t B, int32_t Hq,
+                    int32_t Hkv, const int32_t* seq_lens, int32_t max_seq_len, int32_t D, float scale,
+                    int32_t n_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  fd_status st = check_shape(B, Hq, Hkv, D);
+  if (st != FD_OK) return st;
+  if (!q || !out || !workspace || !aligned16(q) || !aligned16(out) || !aligned16(workspace))
+    return FD_ERR_INVALID_ARG;
+  if (n_splits < 0 || n_splits > 65535) return FD_ERR_INVALID_ARG;
+  if ((st = check_kv(kv, B, Hkv, max_seq_len)) != FD_OK) return st;
+  const Groups gr = make_groups(Hq, Hkv);
+  const int64_t pairs = (int64_t)B * gr.hv;
+  int sms = 0;
+  if (n_splits == 0) {
+    if (!sm_count(&sms)) return FD_ERR_CUDA;
+    if (B > FD_AUTO_MAX_BATCH || pairs > kMaxFusedPairs) n_splits = fallback_splits(B, gr.hv, max_seq_len, sms);
+  }
+  const WsLayout w = ws_layout(B, Hq, Hkv, D, n_splits, sms);
+  if (workspace_bytes < w.total) return FD_ERR_WORKSPACE_TOO_SMALL;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  SplitParams p = base_params(q, kv, B, Hq, Hkv, seq_lens, max_seq_len, scale);
+  p.out = out;
+  p.lse = lse;
+  p.o_part = reinterpret_cast<float*>(ws + w.o);
+  p.m_part = reinterpret_cast<float*>(ws + w.m);
+  p.l_part = reinterpret_cast<float*>(ws + w.l);
+  p.err = reinterpret_cast<unsigned*>(ws + w.err);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (n_splits == 0) {
+    p.n_splits = 0;
+    p.counters = reinterpret_cast<int*>(ws + w.counters);
+    return launch(kv, D, p, dim3((unsigned)sms, 1, 1), s);
+  }
+  p.n_splits = n_splits;
+  p.split_tokens = max_seq_len > 0 ? explicit_split_size(max_seq_len, n_splits) : kSplitAlign;
+  const dim3 grid((unsigned)pairs, (unsigned)n_splits, 1);
+  if (pairs <= kMaxFusedPairs) {
+    p.counters = reinterpret_cast<int*>(ws + w.counters);
+    return launch(kv, D, p, grid, s);
+  }
+  // Too many sequences for the counter region: split, then a separate merge.
+  p.counters = nullptr;
+  if ((st = launch(kv, D, p, grid, s)) != FD_OK) return st;
+  const cudaError_t e = launch_combine(D, p.o_part, p.m_part, p.l_part, out, lse, B * Hq, n_splits, s);
+  return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+fd_status fd_split_partial(const float* q, const fd_kv_desc* kv, int32_t B, int32_t Hq, int32_t Hkv,
+                           const int32_t* seq_lens, int32_t max_seq_len, int32_t D, float scale,
+                           int32_t n_splits, float* o_part, float* m_part, float* l_part, void* stream) {
+  fd_status st = check_shape(B, Hq, Hkv, D);
+  if (st != FD_OK) return st;
+  if (!q || !o_part || !m_part || !l_part || !aligned16(q) || !aligned16(o_part)) return FD_ERR_INVALID_ARG;
+  if (n_splits < 1 || n_splits > 65535) return FD_ERR_INVALID_ARG;
+  if ((st = check_kv(kv, B, Hkv, max_seq_len)) != FD_OK) return st;
+  SplitParams p = base_params(q, kv, B, Hq, Hkv, seq_lens, max_seq_len, scale);
+  p.o_part = o_part;
+  p.m_part = m_part;
+  p.l_part = l_part;
+  p.n_splits = n_splits;
+  p.split_tokens = max_seq_len > 0 ? explicit_split_size(max_seq_len, n_splits) : kSplitAlign;
+  const dim3 grid((unsigned)(B * p.hv), (unsigned)n_splits, 1);
+  return launch(kv, D, p, grid, (cudaStream_t)stream);
+}
+
+fd_status fd_combine(const float* o_part, const float* m_part, const float* l_part, float* out, float* lse,
+                     int32_t B, int32_t Hq, int32_t D, int32_t n_splits, void* stream) {
+  if (!o_part || !m_part || !l_part || !out || B < 1 || Hq < 1 || n_splits < 1) return FD_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FD_ERR_UNSUPPORTED;
+  if (!aligned16(o_part) || !aligned16(out)) return FD_ERR_INVALID_ARG;
+  if ((int64_t)B * Hq > ((int64_t)1 << 31) - 4) return FD_ERR_UNSUPPORTED;
+  cudaError_t e = launch_combine(D, o_part, m_part, l_part, out, lse, B * Hq, n_splits, (cudaStream_t)stream);
+  return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+fd_status fd_decode_host(const float* q_host, const fd_kv_desc* kv, float* out_host, float* lse_host, int32_t B,
+                         int32_t Hq, int32_t Hkv, const int32_t* seq_lens_host, int32_t max_seq_len, int32_t D,
+                         float scale, int32_t n_splits, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  fd_status st = check_shape(B, Hq, Hkv, D);
+  if (st != FD_OK) return st;
+  if (!q_host || !out_host || !workspace) return FD_ERR_INVALID_ARG;
+  if (n_splits < 0 || n_splits > 65535) return FD_ERR_INVALID_ARG;
+  int grid_ctas = 0;
+  if (n_splits == 0 && !sm_count(&grid_ctas)) return FD_ERR_CUDA;
+  int n_eff = n_splits;
+  const Groups gr = make_groups(Hq, Hkv);
+  if (n_splits == 0 && (B > FD_AUTO_MAX_BATCH || (int64_t)B * gr.hv > kMaxFusedPairs))
+    n_eff = fallback_splits(B, gr.hv, max_seq_len, grid_ctas);
+  const WsLayout w = ws_layout(B, Hq, Hkv, D, n_eff, grid_ctas);
+  if (workspace_bytes < w.total) return FD_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = (cudaStream_t)stream;
+  float* q_dev = reinterpret_cast<float*>(ws + w.q_stage);
+  float* out_dev = reinterpret_cast<float*>(ws + w.out_stage);
+  float* lse_dev = reinterpret_cast<float*>(ws + w.lse_stage);
+  int32_t* len_dev = reinterpret_cast<int32_t*>(ws + w.len_stage);
+  const size_t qbytes = (size_t)B * Hq * D * 4;
+  if (cudaMemcpyAsync(q_dev, q_host, qbytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return FD_ERR_CUDA;
+  if (seq_lens_host &&
+      cudaMemcpyAsync(len_dev, seq_lens_host, (size_t)B * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return FD_ERR_CUDA;
+  st = fd_decode(q_dev, kv, out_dev, lse_host ? lse_dev : nullptr, B, Hq, Hkv, seq_lens_host ? len_dev : nullptr,
+                 max_seq_len, D, scale, n_splits, workspace, workspace_bytes, stream);
+  if (st != FD_OK) return st;
+  if (cudaMemcpyAsync(out_host, out_dev, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return FD_ERR_CUDA;
+  if (lse_host &&
+      cudaMemcpyAsync(lse_host, lse_dev, (size_t)B * Hq * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FD_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+int64_t fd_plan_pieces(int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_lens_host, int32_t max_seq_len,
+                       int32_t n_splits, int32_t grid, int32_t* pieces, int64_t capacity) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_seq_len < 0 || n_splits < 0) return -1;
+  const Groups gr = make_groups(Hq, Hkv);
+  std::vector<int32_t> ln(B), pre(B + 1, 0);
+  for (int b = 0; b < B; ++b) ln[b] = clamp_len(seq_lens_host ? seq_lens_host[b] : max_seq_len, max_seq_len);
+  for (int b = 0; b < B; ++b) pre[b + 1] = pre[b] + ceil_div(ln[b], kPlanTile);
+  int64_t count = 0;
+  auto emit = [&](int32_t cta, const Piece& pc, int32_t npieces) {
+    if (pieces && count < capacity) {
+      int32_t* r = pieces + count * 7;
+      r[0] = cta;
+      r[1] = pc.b;
+      r[2] = pc.vkv;
+      r[3] = pc.tok_begin;
+      r[4] = pc.tok_end;
+      r[5] = pc.slot;
+      r[6] = npieces;
+    }
+    ++count;
+  };
+  if (n_splits == 0) {
+    if (grid < 1) return -1;
+    HostTiles tl{pre.data(), ln.data()};
+    const int64_t total = (int64_t)gr.hv * pre[B];
+    if (total == 0) return 0;
+    const int32_t used = balanced_ctas(total, grid);
+    for (int32_t cta = 0; cta < used; ++cta) {
+      BalancedWalk<HostTiles> w(tl, B, gr.hv, total, used, cta);
+      while (!w.done()) {
+        const Piece pc = w.next();
+        int32_t first, last;
+        balanced_pair_ctas(tl, gr.hv, total, used, pc.b, pc.vkv, &first, &last);
+        emit(cta, pc, last - first + 1);
+      }
+    }
+  } else {
+    const int32_t S = max_seq_len > 0 ? explicit_split_size(max_seq_len, n_splits) : kSplitAlign;
+    for (int32_t pair = 0; pair < B * gr.hv; ++pair) {
+      for (int32_t s = 0; s < n_splits; ++s) {
+        Piece pc;
+        pc.b = pair / gr.hv;
+        pc.vkv = pair % gr.hv;
+        const int64_t L = ln[pc.b];
+        const int64_t lo = (int64_t)s * S;
+        const int64_t hi = std::min<int64_t>(lo + S, L);
+        pc.tok_begin = (int32_t)std::min<int64_t>(lo, L);
+        pc.tok_end = (int32_t)std::max<int64_t>(hi, pc.tok_begin);
+        pc.slot = s;
+        emit(pair * n_splits + s, pc, n_splits);
+      }
+    }
+  }
+  return count;
+}
+
+}  // extern "C"

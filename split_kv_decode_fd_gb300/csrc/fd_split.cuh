@@ -1,0 +1,718 @@
+// fd_split.cuh -- the split-KV decode kernel for sm_103a (GB300).
+//
+// One CTA streams K/V for one (batch, KV head) run of keys -- or, in the
+// balanced plan, a fixed share of all runs -- and serves every query head of
+// the GQA group from that single read.  Per CTA:
+//
+//   warp W (producer): walks the CTA's pieces and, per stage of kBT keys,
+//     issues 16-row x 128-byte TMA boxes of K and V into a ring of kStages
+//     shared-memory stages (128-byte swizzle), plus one bulk copy of the
+//     piece's q rows.  mbarriers carry the byte counts.
+//   warps 0..W-1 (consumers): warp w owns rows [32w, 32w+32) of every stage.
+//     q.k:  lane = key row; the lane walks its row in 16-byte chunks (the
+//           swizzle makes the 8 rows of each quarter-warp hit distinct banks)
+//           while q is read from shared memory as a broadcast;
+//     softmax: per warp and head, max over the 32 rows, one exp2 per row;
+//           each warp keeps its own running (m, l, O) -- the online softmax
+//           of the fd_split walkthrough, one level per warp;
+//     p.V:  lane = a D/32-wide slice of the output; the warp walks the valid
+//           rows with p broadcast from shared memory.
+//   At the end of a piece the W warp states are merged in shared memory with
+//   the log-sum-exp rule, giving the piece's (O, m, l).  A piece that covers
+//   its whole sequence is normalised and written as the output directly;
+//   otherwise its partial is written and, when the merge is fused, the last
+//   CTA to finish a sequence merges all of its partials (arrival counter,
+//   no waiting on other CTAs).
+//
+// Scores are kept in base 2 (q.k times scale*log2 e); m written to memory is
+// converted back to natural units.  Masking is by index only: rows past the
+// valid length get score -inf and are skipped in p.V, so nothing stored there
+// (even NaN) reaches a sum.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "fd_device.cuh"
+#include "fd_plan.h"
+
+#ifndef FD_USE_FFMA2
+#define FD_USE_FFMA2 1
+#endif
+
+namespace fdk {
+
+constexpr int kAutoMaxBatch = 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct SplitParams {
+  const float* q;          // [B, Hq, D]
+  float* out;              // [B, Hq, D]      (fused merge only)
+  float* lse;              // [B, Hq] or null (fused merge only)
+  float* o_part;           // balanced: [slots, gpad, D]; explicit: [B, Hq, n_splits, D]
+  float* m_part;           // balanced: [slots, gpad];    explicit: [B, Hq, n_splits]
+  float* l_part;
+  int* counters;           // [B * hv] arrival counters; null = write partials only
+  unsigned* err;           // error word or null
+  const int32_t* seq_lens; // [B] or null
+  const int32_t* block_table;
+  int32_t B, Hq, Hkv;
+  int32_t g, gpad, nsub, hv;
+  int32_t max_len;
+  int32_t n_splits;        // 0 = balanced plan
+  int32_t split_tokens;    // explicit plan: S
+  int32_t paged;
+  int32_t page_size, max_pages, num_pages;
+  float qk_scale;          // scale * log2(e)
+};
+
+template <int D_, class KV, int G_>
+struct SplitCfg {
+  static constexpr int D = D_;
+  static constexpr int G = G_;
+  static constexpr int kEs = (int)sizeof(KV);
+  static constexpr bool kBf16 = kEs == 2;
+  static constexpr int kRowBytes = D * kEs;
+  static constexpr int kNB = kRowBytes / 128;  // 128-byte column blocks per row
+  static constexpr int kWarps = kRowBytes <= 256 ? 4 : 2;
+  static constexpr int kThreads = 32 * (kWarps + 1);
+  static constexpr int kBT = 32 * kWarps;      // keys per stage
+  static constexpr int kTileBytes = kBT * kRowBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kStagesFit = 196608 / kStageBytes;
+  static constexpr int kStages = kStagesFit > 4 ? 4 : kStagesFit;
+  static constexpr int kEPL = D / 32;          // output elements per lane in p.V
+  static constexpr int kChunkElems = 16 / kEs; // elements per 16-byte chunk
+  static constexpr int kAcc = G >= 4 ? 1 : 4 / G;
+  static constexpr int kBoxBytes = 16 * 128;
+  static_assert(kNB >= 1 && kStages >= 2, "unsupported row size");
+
+  // shared-memory layout (byte offsets from a 1024-aligned base)
+  static constexpr int kQOff = kStages * kStageBytes;
+  static constexpr int kQBytes = G * D * 4;
+  static constexpr int kUOff = kQOff + 2 * kQBytes;
+  static constexpr int kPBytes = kWarps * 32 * G * 8;
+  static constexpr int kObBytes = kWarps * G * D * 4;
+  static constexpr int kUBytes = kPBytes > kObBytes ? kPBytes : kObBytes;
+  static constexpr int kMlOff = kUOff + kUBytes;
+  static constexpr int kFinOff = kMlOff + kWarps * G * 8;
+  static constexpr int kLenOff = kFinOff + G * 8;
+  static constexpr int kPreOff = kLenOff + (kAutoMaxBatch + 4) * 4;
+  static constexpr int kBarOff = kPreOff + (kAutoMaxBatch + 4) * 4;
+  static constexpr int kFlagOff = kBarOff + (2 * kStages + 4) * 8;
+  static constexpr int kBytes = kFlagOff + 16;
+  static constexpr int kSmemAlloc = kBytes + 1024;
+  static_assert(kSmemAlloc <= 232448, "shared memory over the sm_100 limit");
+};
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+#if FD_USE_FFMA2
+  return __ffma2_rn(a, b, c);
+#else
+  return make_float2(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y));
+#endif
+}
+
+__device__ __forceinline__ void raise_error(unsigned* err, unsigned bits) {
+  if (err) atomicOr(err, bits);
+}
+
+// Lengths and per-sequence tile counts seen by every thread of a CTA.
+struct CtaTiles {
+  const int32_t* pre;  // shared: tile prefix per sequence (balanced with lengths)
+  const int32_t* ln;   // shared: clamped lengths
+  int32_t ut, ul;      // uniform tile count / length when no lengths are given
+  int uniform;
+  FD_HD int32_t prefix(int32_t b) const { return uniform ? b * ut : pre[b]; }
+  FD_HD int32_t tiles(int32_t b) const { return uniform ? ut : pre[b + 1] - pre[b]; }
+  FD_HD int32_t len(int32_t b) const { return uniform ? ul : ln[b]; }
+};
+
+// Log-sum-exp merge of `count` split states of one head (the combine
+// walkthrough), by one warp.  Split k lives at o + (base + k*stride)*D and
+// m/l + base + k*stride.  Fixed summation order: bit-reproducible.
+template <int D>
+__device__ __forceinline__ void merge_head(const float* o, const float* m, const float* l, size_t base,
+                                           size_t stride, int count, float* out_row, float* lse_slot,
+                                           int lane) {
+  constexpr int EPL = D / 32;
+  float mx = -INFINITY;
+  for (int k = lane; k < count; k += 32) {
+    const size_t i = base + (size_t)k * stride;
+    if (__ldcg(l + i) > 0.f) mx = fmaxf(mx, __ldcg(m + i));
+  }
+  mx = warp_max(mx);
+  float acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  if (mx == -INFINITY) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) out_row[lane * EPL + e] = 0.f;
+    if (lse_slot && lane == 0) *lse_slot = -INFINITY;
+    return;
+  }
+  float lsum = 0.f;
+  for (int k0 = 0; k0 < count; k0 += 32) {
+    const int k = k0 + lane;
+    float w = 0.f;
+    if (k < count) {
+      const size_t i = base + (size_t)k * stride;
+      const float lk = __ldcg(l + i);
+      if (lk > 0.f) {
+        w = exp2f((__ldcg(m + i) - mx) * kLog2e);
+        lsum = fmaf(w, lk, lsum);
+      }
+    }
+    const int n = count - k0 < 32 ? count - k0 : 32;
+    for (int j = 0; j < n; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      if (wj == 0.f) continue;  // warp-uniform
+      const float* src = o + (base + (size_t)(k0 + j) * stride) * D + lane * EPL;
+      if constexpr (EPL == 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+        acc[0] = fmaf(wj, v.x, acc[0]);
+        acc[1] = fmaf(wj, v.y, acc[1]);
+        acc[2] = fmaf(wj, v.z, acc[2]);
+        acc[3] = fmaf(wj, v.w, acc[3]);
+      } else {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+        acc[0] = fmaf(wj, v.x, acc[0]);
+        acc[1] = fmaf(wj, v.y, acc[1]);
+      }
+    }
+  }
+  const float L = warp_sum(lsum);
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) out_row[lane * EPL + e] = acc[e] / L;
+  if (lse_slot && lane == 0) *lse_slot = mx + logf(L);
+}
+
+// Calls f(piece) for every piece of this CTA, in the same order for every role.
+template <class F>
+__device__ __forceinline__ void for_each_piece(const SplitParams& p, const CtaTiles& tl, int64_t total,
+                                               F&& f) {
+  if (p.n_splits == 0) {
+    const int32_t grid = balanced_ctas(total, (int32_t)gridDim.x);
+    if ((int32_t)blockIdx.x >= grid) return;
+    BalancedWalk<CtaTiles> w(tl, p.B, p.hv, total, grid, (int32_t)blockIdx.x);
+    while (!w.done()) f(w.next());
+  } else {
+    const int32_t pair = blockIdx.x, s = blockIdx.y;
+    Piece pc;
+    pc.b = pair / p.hv;
+    pc.vkv = pair % p.hv;
+    const int32_t L = p.seq_lens ? clamp_len(__ldg(p.seq_lens + pc.b), p.max_len) : p.max_len;
+    const int64_t lo = (int64_t)s * p.split_tokens;
+    const int64_t hi = lo + p.split_tokens < L ? lo + p.split_tokens : L;
+    pc.tok_begin = (int32_t)(lo < L ? lo : L);
+    pc.tok_end = (int32_t)(hi > pc.tok_begin ? hi : pc.tok_begin);
+    pc.slot = s;
+    f(pc);
+  }
+}
+
+// ----------------------------------------------------------------- producer
+template <class C>
+__device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUtensorMap* tv,
+                                              const SplitParams& p, const CtaTiles& tl, int64_t total,
+                                              uint8_t* smem, volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* qfull = empty + C::kStages;
+  uint64_t* qempty = qfull + 2;
+  uint32_t it = 0, qi = 0;
+  bool ok = true;
+  Groups gr;
+  gr.g = p.g;
+  gr.gpad = p.gpad;
+  gr.nsub = p.nsub;
+  gr.hv = p.hv;
+
+  for_each_piece(p, tl, total, [&](const Piece& pc) {
+    if (!ok || pc.tok_end <= pc.tok_begin) return;
+    int32_t head0, nh;
+    vkv_heads(gr, pc.vkv, &head0, &nh);
+    const int32_t kvh = kv_head_of_vkv(gr, pc.vkv);
+    if (lane == 0) {
+      const uint32_t slot = qi & 1;
+      if (!mbar_wait(qempty + slot, ((qi >> 1) & 1) ^ 1)) ok = false;
+      if (ok) {
+        const uint32_t bytes = (uint32_t)nh * C::D * 4;
+        mbar_arrive_expect_tx(qfull + slot, bytes);
+        bulk_load(smem + C::kQOff + slot * C::kQBytes, p.q + ((size_t)pc.b * p.Hq + head0) * C::D, bytes,
+                  qfull + slot);
+      }
+    }
+    ++qi;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    for (int32_t t0 = pc.tok_begin; ok && t0 < pc.tok_end; t0 += C::kBT, ++it) {
+      const int32_t nvalid = pc.tok_end - t0 < C::kBT ? pc.tok_end - t0 : C::kBT;
+      const int32_t nbox = ceil_div(nvalid, 16);
+      int32_t page = 0;
+      bool mine = lane < nbox;
+      if (mine && p.paged) {
+        const int32_t tok = t0 + 16 * lane;
+        page = __ldg(p.block_table + (size_t)pc.b * p.max_pages + tok / p.page_size);
+        if (page < 0 || page >= p.num_pages) {
+          raise_error(p.err, kErrBadIndex);
+          mine = false;
+        }
+      }
+      const unsigned issue = __ballot_sync(0xffffffffu, mine);
+      const uint32_t stage = it % C::kStages;
+      const uint32_t phase = (it / C::kStages) & 1;
+      if (lane == 0) {
+        if (*abort_flag || !mbar_wait(empty + stage, phase ^ 1)) {
+          ok = false;
+        } else {
+          mbar_arrive_expect_tx(full + stage, (uint32_t)__popc(issue) * C::kNB * 2 * C::kBoxBytes);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (mine) {
+        uint8_t* kdst = smem + stage * C::kStageBytes + lane * C::kBoxBytes;
+        uint8_t* vdst = kdst + C::kTileBytes;
+#pragma unroll
+        for (int nb = 0; nb < C::kNB; ++nb) {
+          const int32_t x = nb * (128 / C::kEs);
+          const int32_t off = nb * C::kBT * 128;
+          if (p.paged) {
+            const int32_t row = (t0 + 16 * lane) % p.page_size;
+            tma_load_4d(kdst + off, tk, full + stage, x, row, kvh, page);
+            tma_load_4d(vdst + off, tv, full + stage, x, row, kvh, page);
+          } else {
+            const int32_t z = pc.b * p.Hkv + kvh;
+            tma_load_3d(kdst + off, tk, full + stage, x, t0 + 16 * lane, z);
+            tma_load_3d(vdst + off, tv, full + stage, x, t0 + 16 * lane, z);
+          }
+        }
+      }
+    }
+  });
+  if (!ok) {
+    raise_error(p.err, kErrTimeout);
+    *abort_flag = 1;
+  }
+  // Do not leave while copies this warp issued may still be landing.
+  if (lane == 0) {
+    const uint32_t n = it < (uint32_t)C::kStages ? it : (uint32_t)C::kStages;
+    for (uint32_t j = it - n; j < it; ++j) {
+      if (!mbar_wait(full + (j % C::kStages), (j / C::kStages) & 1)) raise_error(p.err, kErrTimeout);
+    }
+  }
+}
+
+// ----------------------------------------------------------------- consumers
+template <class C, bool kFull>
+__device__ __forceinline__ void pv_rows(uint32_t vbase, const uint32_t* voff, uint32_t pbase, int nv,
+                                        float2 (&o)[C::G][C::kEPL / 2]) {
+  constexpr int G = C::G;
+  for (int t8 = 0; t8 < nv; t8 += 8) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t = t8 + j;
+      if (kFull || t < nv) {
+        const uint32_t a = vbase + t * 128 + voff[j];
+        float vf[C::kEPL];
+        if constexpr (C::kBf16) {
+          if constexpr (C::kEPL == 4) {
+            const uint2 w = lds64u(a);
+            vf[0] = bf16_lo(w.x);
+            vf[1] = bf16_hi(w.x);
+            vf[2] = bf16_lo(w.y);
+            vf[3] = bf16_hi(w.y);
+          } else {
+            const uint32_t w = lds32u(a);
+            vf[0] = bf16_lo(w);
+            vf[1] = bf16_hi(w);
+          }
+        } else {
+          if constexpr (C::kEPL == 4) {
+            const float4 w = lds128(a);
+            vf[0] = w.x;
+            vf[1] = w.y;
+            vf[2] = w.z;
+            vf[3] = w.w;
+          } else {
+            const uint2 w = lds64u(a);
+            vf[0] = __uint_as_float(w.x);
+            vf[1] = __uint_as_float(w.y);
+          }
+        }
+        const uint32_t prow = pbase + t * (G * 8);
+        if constexpr (G == 1) {
+          const uint2 pw = lds64u(prow);
+          const float2 pp = make_float2(__uint_as_float(pw.x), __uint_as_float(pw.y));
+#pragma unroll
+          for (int i = 0; i < C::kEPL / 2; ++i) o[0][i] = fma2(make_float2(vf[2 * i], vf[2 * i + 1]), pp, o[0][i]);
+        } else {
+#pragma unroll
+          for (int h = 0; h < G; h += 2) {
+            const float4 pq = lds128(prow + h * 8);
+            const float2 p0 = make_float2(pq.x, pq.y), p1 = make_float2(pq.z, pq.w);
+#pragma unroll
+            for (int i = 0; i < C::kEPL / 2; ++i) {
+              const float2 v2 = make_float2(vf[2 * i], vf[2 * i + 1]);
+              o[h][i] = fma2(v2, p0, o[h][i]);
+              o[h + 1][i] = fma2(v2, p1, o[h + 1][i]);
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+template <class C>
+__device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTiles& tl, int64_t total,
+                                               uint8_t* smem, volatile int* abort_flag) {
+  constexpr int G = C::G, D = C::D, W = C::kWarps, EPL = C::kEPL;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  constexpr int kCons = W * 32;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* qfull = empty + C::kStages;
+  uint64_t* qempty = qfull + 2;
+  float* obuf = reinterpret_cast<float*>(smem + C::kUOff);
+  float* mlbuf = reinterpret_cast<float*>(smem + C::kMlOff);
+  float* fin = reinterpret_cast<float*>(smem + C::kFinOff);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::kFlagOff + 4);
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t pbase = sbase + C::kUOff + warp * 32 * G * 8;
+  const bool balanced = p.n_splits == 0;
+  const bool fused = p.counters != nullptr;
+
+  Groups gr;
+  gr.g = p.g;
+  gr.gpad = p.gpad;
+  gr.nsub = p.nsub;
+  gr.hv = p.hv;
+
+  // Balanced plan: sequences with no keys own no tile; CTA b % grid writes their outputs.
+  if (balanced && fused) {
+    for (int32_t b = blockIdx.x; b < p.B; b += gridDim.x) {
+      if (tl.len(b) != 0) continue;
+      for (int i = tid; i < p.Hq * D; i += kCons) p.out[(size_t)b * p.Hq * D + i] = 0.f;
+      if (p.lse)
+        for (int i = tid; i < p.Hq; i += kCons) p.lse[(size_t)b * p.Hq + i] = -INFINITY;
+    }
+  }
+
+  // Per-lane constants of the swizzled addressing.
+  const uint32_t xr = lane & 7;
+  // p.V: this lane's slice of a row
+  const int e_byte = lane * EPL * C::kEs;     // byte offset in the row
+  const int e_nb = e_byte / 128;               // column block
+  const int e_chunk = (e_byte % 128) / 16;     // 16-byte chunk within the block
+  const int e_in = e_byte % 16;                // byte within the chunk
+  uint32_t voff[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) voff[j] = ((e_chunk ^ j) << 4) + e_in;
+
+  uint32_t it = 0, qi = 0;
+  bool ok = true;
+
+  for_each_piece(p, tl, total, [&](const Piece& pc) {
+    int32_t head0, nh;
+    vkv_heads(gr, pc.vkv, &head0, &nh);
+    const bool nonempty = pc.tok_end > pc.tok_begin;
+    float m[G], l[G];
+    float2 o[G][EPL / 2];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int i = 0; i < EPL / 2; ++i) o[h][i] = make_float2(0.f, 0.f);
+    }
+    const uint32_t qslot = qi & 1;
+    if (nonempty && ok) {
+      if (!mbar_wait(qfull + qslot, (qi >> 1) & 1)) {
+        ok = false;
+        *abort_flag = 1;
+      }
+      const uint32_t qaddr = sbase + C::kQOff + qslot * C::kQBytes;
+      for (int32_t t0 = pc.tok_begin; ok && t0 < pc.tok_end; t0 += C::kBT, ++it) {
+        const uint32_t stage = it % C::kStages;
+        if (*abort_flag || !mbar_wait(full + stage, (it / C::kStages) & 1)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        const int32_t nvalid = pc.tok_end - t0 < C::kBT ? pc.tok_end - t0 : C::kBT;
+        int nv = nvalid - 32 * warp;
+        nv = nv < 0 ? 0 : (nv > 32 ? 32 : nv);
+        if (nv > 0) {
+          const uint32_t kst = sbase + stage * C::kStageBytes;
+          const uint32_t vst = kst + C::kTileBytes;
+          // ---- q.k, lane = row
+          float2 acc[G][C::kAcc];
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int a = 0; a < C::kAcc; ++a) acc[h][a] = make_float2(0.f, 0.f);
+          const uint32_t krow = kst + (32 * warp + lane) * 128;
+#pragma unroll
+          for (int nb = 0; nb < C::kNB; ++nb) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int a = (nb * 8 + c) % C::kAcc;
+              const uint4 kw = lds128u(krow + nb * C::kBT * 128 + ((c ^ xr) << 4));
+              const int d0 = nb * (128 / C::kEs) + c * C::kChunkElems;
+              if constexpr (C::kBf16) {
+                const float2 k01 = make_float2(bf16_lo(kw.x), bf16_hi(kw.x));
+                const float2 k23 = make_float2(bf16_lo(kw.y), bf16_hi(kw.y));
+                const float2 k45 = make_float2(bf16_lo(kw.z), bf16_hi(kw.z));
+                const float2 k67 = make_float2(bf16_lo(kw.w), bf16_hi(kw.w));
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                  const float4 qa = lds128(qaddr + (h * D + d0) * 4);
+                  const float4 qb = lds128(qaddr + (h * D + d0 + 4) * 4);
+                  acc[h][a] = fma2(k01, make_float2(qa.x, qa.y), acc[h][a]);
+                  acc[h][a] = fma2(k23, make_float2(qa.z, qa.w), acc[h][a]);
+                  acc[h][a] = fma2(k45, make_float2(qb.x, qb.y), acc[h][a]);
+                  acc[h][a] = fma2(k67, make_float2(qb.z, qb.w), acc[h][a]);
+                }
+              } else {
+                const float2 k01 = make_float2(__uint_as_float(kw.x), __uint_as_float(kw.y));
+                const float2 k23 = make_float2(__uint_as_float(kw.z), __uint_as_float(kw.w));
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                  const float4 qa = lds128(qaddr + (h * D + d0) * 4);
+                  acc[h][a] = fma2(k01, make_float2(qa.x, qa.y), acc[h][a]);
+                  acc[h][a] = fma2(k23, make_float2(qa.z, qa.w), acc[h][a]);
+                }
+              }
+            }
+          }
+          // ---- online softmax over this warp's rows
+          const bool valid = lane < nv;
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float s = 0.f;
+#pragma unroll
+            for (int a = 0; a < C::kAcc; ++a) s += acc[h][a].x + acc[h][a].y;
+            s = valid ? s * p.qk_scale : -INFINITY;
+            const float mn = fmaxf(m[h], warp_max(s));
+            const float alpha = exp2f(m[h] - mn);
+            const float pr = exp2f(s - mn);
+            l[h] = fmaf(l[h], alpha, pr);
+            const float2 al = make_float2(alpha, alpha);
+#pragma unroll
+            for (int i = 0; i < EPL / 2; ++i) o[h][i] = make_float2(o[h][i].x * al.x, o[h][i].y * al.y);
+            m[h] = mn;
+            // p, duplicated as a pair, for the broadcast reads of p.V
+            *reinterpret_cast<float2*>(smem + C::kUOff + (warp * 32 + lane) * G * 8 + h * 8) =
+                make_float2(pr, pr);
+          }
+          __syncwarp();
+          // ---- p.V, lane = output slice
+          const uint32_t vbase = vst + e_nb * C::kBT * 128 + (32 * warp) * 128;
+          if (nv == 32)
+            pv_rows<C, true>(vbase, voff, pbase, 32, o);
+          else
+            pv_rows<C, false>(vbase, voff, pbase, nv, o);
+          __syncwarp();
+        }
+        if (lane == 0) mbar_arrive(empty + stage);
+      }
+    }
+
+    // ---- merge the W warp states of this piece
+    float lw[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) lw[h] = warp_sum(l[h]);
+    named_barrier(1, kCons);  // every warp is past its last p.V: the p buffers may be reused
+    if (nonempty && tid == 0) mbar_arrive(qempty + qslot);
+    if (nonempty) ++qi;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float* dst = obuf + (warp * G + h) * D + lane * EPL;
+#pragma unroll
+      for (int i = 0; i < EPL / 2; ++i) reinterpret_cast<float2*>(dst)[i] = o[h][i];
+      if (lane == 0) {
+        mlbuf[(warp * G + h) * 2] = m[h];
+        mlbuf[(warp * G + h) * 2 + 1] = lw[h];
+      }
+    }
+    named_barrier(1, kCons);
+    if (tid < G) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < W; ++w) M = fmaxf(M, mlbuf[(w * G + tid) * 2]);
+      float L = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          const float mw = mlbuf[(w * G + tid) * 2];
+          if (mw != -INFINITY) L = fmaf(exp2f(mw - M), mlbuf[(w * G + tid) * 2 + 1], L);
+        }
+      }
+      fin[tid * 2] = M;
+      fin[tid * 2 + 1] = L;
+    }
+    named_barrier(1, kCons);
+
+    // Does this piece hold the whole sequence?  Then it is the output.
+    int npieces = 1;
+    const int32_t pair = pc.b * p.hv + pc.vkv;
+    if (balanced) {
+      int32_t first, last;
+      balanced_pair_ctas(tl, p.hv, total, balanced_ctas(total, (int32_t)gridDim.x), pc.b, pc.vkv, &first,
+                         &last);
+      npieces = last - first + 1;
+    } else {
+      npieces = p.n_splits;
+    }
+    const bool final_here = fused && npieces == 1;
+
+    for (int idx = tid; idx < G * D; idx += kCons) {
+      const int h = idx / D, d = idx % D;
+      if (h >= nh) continue;
+      const float M = fin[h * 2];
+      float acc = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          const float mw = mlbuf[(w * G + h) * 2];
+          if (mw != -INFINITY) acc = fmaf(exp2f(mw - M), obuf[(w * G + h) * D + d], acc);
+        }
+      }
+      if (final_here) {
+        const float L = fin[h * 2 + 1];
+        p.out[((size_t)pc.b * p.Hq + head0 + h) * D + d] = M == -INFINITY ? 0.f : acc / L;
+      } else if (balanced) {
+        p.o_part[((size_t)pc.slot * G + h) * D + d] = acc;
+      } else {
+        p.o_part[(((size_t)pc.b * p.Hq + head0 + h) * p.n_splits + pc.slot) * D + d] = acc;
+      }
+    }
+    if (tid < nh) {
+      const float M = fin[tid * 2], L = fin[tid * 2 + 1];
+      const float m_nat = M == -INFINITY ? -INFINITY : M * kLn2;
+      if (final_here) {
+        if (p.lse) p.lse[(size_t)pc.b * p.Hq + head0 + tid] = M == -INFINITY ? -INFINITY : m_nat + logf(L);
+      } else {
+        const size_t i = balanced ? (size_t)pc.slot * G + tid
+                                  : ((size_t)pc.b * p.Hq + head0 + tid) * p.n_splits + pc.slot;
+        p.m_part[i] = m_nat;
+        p.l_part[i] = L;
+      }
+    }
+
+    if (fused && !final_here) {
+      __threadfence();
+      named_barrier(1, kCons);
+      if (tid == 0) *last_flag = (atomicAdd(p.counters + pair, 1) == npieces - 1) ? 1 : 0;
+      named_barrier(1, kCons);
+      if (*last_flag) {
+        __threadfence();
+        size_t base0, stride;
+        int count;
+        if (balanced) {
+          int32_t first, last;
+          balanced_pair_ctas(tl, p.hv, total, balanced_ctas(total, (int32_t)gridDim.x), pc.b, pc.vkv, &first,
+                         &last);
+          base0 = (size_t)(pair + first) * G;
+          stride = G;
+          count = last - first + 1;
+        } else {
+          base0 = ((size_t)pc.b * p.Hq + head0) * p.n_splits;
+          stride = 1;
+          count = p.n_splits;
+        }
+        for (int h = warp; h < nh; h += W) {
+          const size_t base = balanced ? base0 + h : base0 + (size_t)h * p.n_splits;
+          merge_head<D>(p.o_part, p.m_part, p.l_part, base, stride, count,
+                        p.out + ((size_t)pc.b * p.Hq + head0 + h) * D,
+                        p.lse ? p.lse + (size_t)pc.b * p.Hq + head0 + h : nullptr, lane);
+        }
+        if (tid == 0) p.counters[pair] = 0;  // ready for the next call
+      }
+    }
+    named_barrier(1, kCons);  // shared merge buffers are free again
+  });
+  if (!ok) {
+    raise_error(p.err, kErrTimeout);
+    *abort_flag = 1;
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    fd_split_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                    const SplitParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kFlagOff);
+  int32_t* lens = reinterpret_cast<int32_t*>(smem + C::kLenOff);
+  int32_t* pre = reinterpret_cast<int32_t*>(smem + C::kPreOff);
+
+  if (tid == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bars + s, 1);                         // full: producer's expect_tx arrival
+      mbar_init(bars + C::kStages + s, C::kWarps);    // empty: one arrival per consumer warp
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars + 2 * C::kStages + i, 1);        // q full
+      mbar_init(bars + 2 * C::kStages + 2 + i, 1);    // q empty
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == C::kWarps && (tid & 31) == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  // q rows past the live heads of a group must hold finite values.
+  for (int i = tid; i < 2 * C::G * C::D; i += C::kThreads)
+    reinterpret_cast<float*>(smem + C::kQOff)[i] = 0.f;
+
+  CtaTiles tl;
+  tl.pre = pre;
+  tl.ln = lens;
+  tl.ul = p.max_len;
+  tl.ut = ceil_div(p.max_len, kPlanTile);
+  tl.uniform = 1;
+  if (p.n_splits == 0 && p.seq_lens != nullptr) {
+    tl.uniform = 0;
+    for (int b = tid; b < p.B; b += C::kThreads) lens[b] = clamp_len(__ldg(p.seq_lens + b), p.max_len);
+    __syncthreads();
+    if (warp == 0) {
+      const int lane = tid & 31;
+      const int per = ceil_div(p.B, 32);
+      const int lo = lane * per;
+      const int hi = lo + per < p.B ? lo + per : p.B;
+      int sum = 0;
+      for (int b = lo; b < hi; ++b) sum += ceil_div(lens[b], kPlanTile);
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      int run = incl - sum;
+      for (int b = lo; b < hi; ++b) {
+        pre[b] = run;
+        run += ceil_div(lens[b], kPlanTile);
+      }
+      if (lane == 31) pre[p.B] = incl;
+    }
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncthreads();
+  const int64_t total = (int64_t)p.hv * tl.prefix(p.B);
+
+  if (warp == C::kWarps)
+    producer_warp<C>(&tmap_k, &tmap_v, p, tl, total, smem, abort_flag);
+  else
+    consumer_warps<C>(p, tl, total, smem, abort_flag);
+}
+
+}  // namespace fdk

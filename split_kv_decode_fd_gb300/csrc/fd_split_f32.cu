@@ -1,0 +1,9 @@
+// fd_split_f32.cu -- split kernels for fp32 K/V caches (D = 64, 128; 1..8 heads per CTA).
+#include "fd_split_launch.cuh"
+
+namespace fdk {
+cudaError_t launch_split_f32(int D, int gpad, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const SplitParams& p, dim3 grid, cudaStream_t stream) {
+  return launch_split_dispatch<float>(D, gpad, tk, tv, p, grid, stream);
+}
+}  // namespace fdk
