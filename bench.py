@@ -46,11 +46,15 @@ def parse_args():
 
 
 # ------------------------------------------------------------------ helpers
+KERNEL_SOURCES = ("fd_split.cuh", "fd_device.cuh", "fd_plan.h", "fd_split_launch.cuh", "fd_split_bf16.cu",
+                  "fd_split_f32.cu")
+
+
 def source_hash() -> str:
+    """Hash of the device code of the split kernel (host-only files excluded)."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "split_kv_decode_fd_gb300", "csrc", "*"))):
-        if p.endswith((".cu", ".cuh", ".h")):
-            h.update(open(p, "rb").read())
+    for name in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "split_kv_decode_fd_gb300", "csrc", name), "rb").read())
     return h.hexdigest()[:12]
 
 
@@ -72,9 +76,10 @@ def recorded_traffic(workload_name: str):
             continue
         vals = {}
         for line in txt.splitlines():
-            if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha")):
+            line = line.strip().lstrip("-* ").strip()
+            if ":" in line and line.startswith(("traffic_bytes_per_launch", "source_sha")):
                 k, v = line.split(":", 1)
-                vals[k.strip("-* `")] = v.strip(" `")
+                vals[k.strip(" `")] = v.strip(" `")
         if vals.get("source_sha") == source_hash() and "traffic_bytes_per_launch" in vals:
             try:
                 return int(float(vals["traffic_bytes_per_launch"]))
