@@ -193,6 +193,35 @@ FD_API fd_status fd_decode_host(const float* q_host, const fd_kv_desc* kv, float
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fd_decode without a workspace, for callers that cannot allocate device
+ * memory: code handed only its input and output buffers by a host framework
+ * (plugin or custom-operator interfaces that own every allocation), and code
+ * that must not call cudaMalloc on its path because cudaMalloc can synchronise
+ * the device and stall work running on other streams.  The pages have no
+ * counterpart to this call; it is a deployment variant of fd_decode.
+ *   Arguments as in fd_decode, minus the workspace.  The scratch (error word,
+ *   merge counters, split partials) is one file-scope device array of
+ *   FD_STATIC_SCRATCH_BYTES inside the library; every GPU that loads the
+ *   library holds it until the process exits.
+ *   The first call on a device looks the array's device address up
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   Returns FD_ERR_WORKSPACE_TOO_SMALL, before any launch, when the problem
+ *   needs more scratch than the array holds (fd_workspace_bytes of the same
+ *   problem, minus its host-staging part, is the amount needed).
+ *   Allocates nothing: no cudaMalloc or cudaFree.  Each call clears the error
+ *   word and the counters (cudaMemsetAsync) and then launches as fd_decode.
+ *   All calls share the one array, and it keeps the last call's contents:
+ *   calls that overlap on the GPU (different streams, other host threads)
+ *   race on it and must be ordered by the caller.
+ */
+#define FD_STATIC_SCRATCH_BYTES (16u << 20)
+
+FD_API fd_status fd_decode_static(const float* q, const fd_kv_desc* kv, float* out, float* lse, int32_t B,
+                                  int32_t Hq, int32_t Hkv, const int32_t* seq_lens, int32_t max_seq_len,
+                                  int32_t D, float scale, int32_t n_splits, void* stream);
+
+/*
  * Host-side description of the work decomposition, for inspection and tests
  * (touches no GPU).  Enumerates every split piece that fd_decode would run
  * for these lengths on `grid` CTAs (FD_SPLITS_AUTO) or for n_splits > 0.

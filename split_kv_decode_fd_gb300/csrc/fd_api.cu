@@ -441,3 +441,88 @@ int64_t fd_plan_pieces(int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_le
 }
 
 }  // extern "C"
+
+// --------------------------------------------------------------------------
+// fd_decode_static: fd_decode for callers that cannot allocate device memory.
+//
+// The scratch that fd_decode takes from the caller's workspace (error word,
+// arrival counters, split partials) lives here in one file-scope device array
+// instead.  It is loaded with the library, so every GPU that loads the library
+// holds these bytes until the process exits.
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)FD_STATIC_SCRATCH_BYTES;
+static_assert(kStaticScratchBytes % 256 == 0, "scratch size must keep 256-byte alignment");
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch on each device, looked up once per device
+// (the host-side symbol is only a stand-in and must never reach a kernel).
+std::mutex g_static_mutex;
+void* g_static_ptr[64] = {};
+
+fd_status static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FD_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return FD_ERR_CUDA;
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return FD_OK;
+}
+
+}  // namespace
+
+extern "C" fd_status fd_decode_static(const float* q, const fd_kv_desc* kv, float* out, float* lse, int32_t B,
+                                      int32_t Hq, int32_t Hkv, const int32_t* seq_lens, int32_t max_seq_len,
+                                      int32_t D, float scale, int32_t n_splits, void* stream) {
+  fd_status st = check_shape(B, Hq, Hkv, D);
+  if (st != FD_OK) return st;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return FD_ERR_INVALID_ARG;
+  if (n_splits < 0 || n_splits > 65535) return FD_ERR_INVALID_ARG;
+  if ((st = check_kv(kv, B, Hkv, max_seq_len)) != FD_OK) return st;
+  const Groups gr = make_groups(Hq, Hkv);
+  const int64_t pairs = (int64_t)B * gr.hv;
+  int sms = 0;
+  if (n_splits == 0) {
+    if (!sm_count(&sms)) return FD_ERR_CUDA;
+    if (B > FD_AUTO_MAX_BATCH || pairs > kMaxFusedPairs) n_splits = fallback_splits(B, gr.hv, max_seq_len, sms);
+  }
+  const WsLayout w = ws_layout(B, Hq, Hkv, D, n_splits, sms);
+  // Only the scratch part of the layout is used here (no host staging area).
+  if (w.q_stage > kStaticScratchBytes) return FD_ERR_WORKSPACE_TOO_SMALL;
+  void* base = nullptr;
+  if ((st = static_scratch(&base)) != FD_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(base);
+  cudaStream_t s = (cudaStream_t)stream;
+  // The array keeps the previous call's contents; the error word and the
+  // arrival counters must start at zero.
+  if (cudaMemsetAsync(ws, 0, w.o, s) != cudaSuccess) return FD_ERR_CUDA;
+
+  SplitParams p = base_params(q, kv, B, Hq, Hkv, seq_lens, max_seq_len, scale);
+  p.out = out;
+  p.lse = lse;
+  p.o_part = reinterpret_cast<float*>(ws + w.o);
+  p.m_part = reinterpret_cast<float*>(ws + w.m);
+  p.l_part = reinterpret_cast<float*>(ws + w.l);
+  p.err = reinterpret_cast<unsigned*>(ws + w.err);
+  if (n_splits == 0) {
+    p.n_splits = 0;
+    p.counters = reinterpret_cast<int*>(ws + w.counters);
+    return launch(kv, D, p, dim3((unsigned)sms, 1, 1), s);
+  }
+  p.n_splits = n_splits;
+  p.split_tokens = max_seq_len > 0 ? explicit_split_size(max_seq_len, n_splits) : kSplitAlign;
+  const dim3 grid((unsigned)pairs, (unsigned)n_splits, 1);
+  if (pairs <= kMaxFusedPairs) {
+    p.counters = reinterpret_cast<int*>(ws + w.counters);
+    return launch(kv, D, p, grid, s);
+  }
+  p.counters = nullptr;
+  if ((st = launch(kv, D, p, grid, s)) != FD_OK) return st;
+  const cudaError_t e = launch_combine(D, p.o_part, p.m_part, p.l_part, out, lse, B * Hq, n_splits, s);
+  return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}

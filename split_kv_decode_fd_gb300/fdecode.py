@@ -17,7 +17,7 @@ import numpy as np
 
 __all__ = [
     "FdError", "KvDesc", "library_path", "load_library", "workspace_bytes", "split_size", "plan_pieces",
-    "Workspace", "decode", "decode_host", "split_partial", "combine", "workspace_status",
+    "Workspace", "decode", "decode_host", "decode_static", "split_partial", "combine", "workspace_status",
 ]
 
 FD_OK, FD_ERR_INVALID_ARG, FD_ERR_UNSUPPORTED, FD_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3
@@ -83,6 +83,8 @@ def load_library(path: Optional[str] = None):
             "fd_decode_host": (ctypes.c_int, [vp, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32, c_i32, f32, c_i32,
                                               vp, c_sz, vp]),
             "fd_plan_pieces": (c_i64, [c_i32, c_i32, c_i32, vp, c_i32, c_i32, c_i32, vp, c_i64]),
+            "fd_decode_static": (ctypes.c_int, [vp, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32, c_i32, f32,
+                                                c_i32, vp]),
             "fd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "fd_version": (c_i32, []),
         }
@@ -240,6 +242,33 @@ def decode(q, k, v, *, seq_lens=None, max_seq_len=None, block_table=None, scale=
                           B, Hq, Hkv, seq_lens.data_ptr() if seq_lens is not None else None, max_seq_len, D,
                           float(scale), int(n_splits), buf.data_ptr(), buf.numel(), _stream_handle(q.device, stream))
     _check(st, "fd_decode")
+    return out, lse
+
+
+def decode_static(q, k, v, *, out, lse=None, seq_lens=None, max_seq_len=None, block_table=None, scale=None,
+                  n_splits=FD_SPLITS_AUTO, stream=None):
+    """``fd_decode_static``: fd_decode for callers that may not allocate device memory.
+
+    The caller passes every buffer (``out`` is required; ``lse`` optional); the
+    library's scratch is a fixed device array inside libfdecode, shared by all
+    calls, so calls must not overlap on the GPU.  Nothing is allocated here.
+    """
+    torch = _torch()
+    _need_cuda(q, "q", torch.float32)
+    _need_cuda(out, "out", torch.float32)
+    kv = _kv_desc(k, v, block_table)
+    B, Hq, Hkv, D, max_seq_len = _geometry(q, k, block_table, seq_lens, max_seq_len)
+    if seq_lens is not None:
+        _need_cuda(seq_lens, "seq_lens", torch.int32)
+    if lse is not None:
+        _need_cuda(lse, "lse", torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    st = _lib().fd_decode_static(q.data_ptr(), ctypes.byref(kv), out.data_ptr(),
+                                 lse.data_ptr() if lse is not None else None, B, Hq, Hkv,
+                                 seq_lens.data_ptr() if seq_lens is not None else None, max_seq_len, D,
+                                 float(scale), int(n_splits), _stream_handle(q.device, stream))
+    _check(st, "fd_decode_static")
     return out, lse
 
 
