@@ -46,7 +46,7 @@ def parse_args():
 
 
 # ------------------------------------------------------------------ helpers
-KERNEL_SOURCES = ("fd_split.cuh", "fd_device.cuh", "fd_plan.h", "fd_split_launch.cuh", "fd_split_bf16.cu",
+KERNEL_SOURCES = ("fd_split.cuh", "fd_split_mma.cuh", "fd_device.cuh", "fd_plan.h", "fd_split_launch.cuh", "fd_split_bf16.cu",
                   "fd_split_f32.cu")
 
 

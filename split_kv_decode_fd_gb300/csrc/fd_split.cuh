@@ -83,8 +83,12 @@ struct SplitCfg {
   static constexpr int kStages = kStagesFit > 4 ? 4 : kStagesFit;
   static constexpr int kEPL = D / 32;          // output elements per lane in p.V
   static constexpr int kChunkElems = 16 / kEs; // elements per 16-byte chunk
-  static constexpr int kAcc = G >= 4 ? 1 : 4 / G;
+  // Independent q.k accumulator chains per head: eight chains in all keep the
+  // packed FMAs of one lane from waiting on each other.
+  static constexpr int kAcc = G >= 8 ? 1 : 8 / G;
   static constexpr int kBoxBytes = 16 * 128;
+  // bf16 caches with eight query heads per CTA run q.k and p.V on mma.sync
+  static constexpr bool kMma = kBf16 && G == 8;
   static_assert(kNB >= 1 && kStages >= 2, "unsupported row size");
 
   // shared-memory layout (byte offsets from a 1024-aligned base)
@@ -305,6 +309,12 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
 }
 
 // ----------------------------------------------------------------- consumers
+// Each consumer warp owns key rows [32w, 32w+32) of every stage and keeps its
+// own running (m, l, O) per head.  Two engines compute a tile: the CUDA-core
+// engine below, and MmaEngine (fd_split_mma.cuh) for bf16 caches with eight
+// query heads per CTA, where q.k and p.V run on mma.sync.  Both publish the
+// warp state the same way, so the merge code is shared.
+
 template <class C, bool kFull>
 __device__ __forceinline__ void pv_rows(uint32_t vbase, const uint32_t* voff, uint32_t pbase, int nv,
                                         float2 (&o)[C::G][C::kEPL / 2]) {
@@ -365,10 +375,135 @@ __device__ __forceinline__ void pv_rows(uint32_t vbase, const uint32_t* voff, ui
   }
 }
 
+// CUDA-core engine.  q.k: lane = key row, 16-byte chunks of the row, q read as
+// a shared-memory broadcast.  p.V: lane = a D/32-wide slice of the output, p
+// broadcast from shared memory.  m, l, O per head; m is warp-uniform.
 template <class C>
+struct CoreEngine {
+  static constexpr int G = C::G, D = C::D, EPL = C::kEPL;
+  float m[G], l[G];
+  float2 o[G][EPL / 2];
+  uint32_t xr, pbase, e_nb;
+  uint32_t voff[8];
+  int warp, lane;
+  uint8_t* smem;
+
+  __device__ __forceinline__ void setup(int warp_, int lane_, uint8_t* smem_) {
+    warp = warp_;
+    lane = lane_;
+    smem = smem_;
+    xr = lane & 7;
+    pbase = smem_addr(smem) + C::kUOff + warp * 32 * G * 8;
+    const int e_byte = lane * EPL * C::kEs;  // this lane's slice of a row, in bytes
+    e_nb = e_byte / 128;                     // column block
+    const int e_chunk = (e_byte % 128) / 16; // 16-byte chunk within the block
+    const int e_in = e_byte % 16;            // byte within the chunk
+#pragma unroll
+    for (int j = 0; j < 8; ++j) voff[j] = ((e_chunk ^ j) << 4) + e_in;
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int i = 0; i < EPL / 2; ++i) o[h][i] = make_float2(0.f, 0.f);
+    }
+  }
+
+  __device__ __forceinline__ void begin(uint32_t, float) {}
+
+  __device__ __forceinline__ void tile(uint32_t kst, uint32_t vst, int nv, uint32_t qaddr, float qk_scale) {
+    // ---- q.k, lane = row
+    float2 acc[G][C::kAcc];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int a = 0; a < C::kAcc; ++a) acc[h][a] = make_float2(0.f, 0.f);
+    const uint32_t krow = kst + (32 * warp + lane) * 128;
+#pragma unroll
+    for (int nb = 0; nb < C::kNB; ++nb) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int a = (nb * 8 + c) % C::kAcc;
+        const uint4 kw = lds128u(krow + nb * C::kBT * 128 + ((c ^ xr) << 4));
+        const int d0 = nb * (128 / C::kEs) + c * C::kChunkElems;
+        if constexpr (C::kBf16) {
+          const float2 k01 = make_float2(bf16_lo(kw.x), bf16_hi(kw.x));
+          const float2 k23 = make_float2(bf16_lo(kw.y), bf16_hi(kw.y));
+          const float2 k45 = make_float2(bf16_lo(kw.z), bf16_hi(kw.z));
+          const float2 k67 = make_float2(bf16_lo(kw.w), bf16_hi(kw.w));
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float4 qa = lds128(qaddr + (h * D + d0) * 4);
+            const float4 qb = lds128(qaddr + (h * D + d0 + 4) * 4);
+            acc[h][a] = fma2(k01, make_float2(qa.x, qa.y), acc[h][a]);
+            acc[h][a] = fma2(k23, make_float2(qa.z, qa.w), acc[h][a]);
+            acc[h][a] = fma2(k45, make_float2(qb.x, qb.y), acc[h][a]);
+            acc[h][a] = fma2(k67, make_float2(qb.z, qb.w), acc[h][a]);
+          }
+        } else {
+          const float2 k01 = make_float2(__uint_as_float(kw.x), __uint_as_float(kw.y));
+          const float2 k23 = make_float2(__uint_as_float(kw.z), __uint_as_float(kw.w));
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float4 qa = lds128(qaddr + (h * D + d0) * 4);
+            acc[h][a] = fma2(k01, make_float2(qa.x, qa.y), acc[h][a]);
+            acc[h][a] = fma2(k23, make_float2(qa.z, qa.w), acc[h][a]);
+          }
+        }
+      }
+    }
+    // ---- online softmax over this warp's rows
+    const bool valid = lane < nv;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float s = 0.f;
+#pragma unroll
+      for (int a = 0; a < C::kAcc; ++a) s += acc[h][a].x + acc[h][a].y;
+      s = valid ? s * qk_scale : -INFINITY;
+      const float mn = fmaxf(m[h], warp_max(s));
+      const float alpha = exp2f(m[h] - mn);
+      const float pr = exp2f(s - mn);
+      l[h] = fmaf(l[h], alpha, pr);
+      const float2 al = make_float2(alpha, alpha);
+#pragma unroll
+      for (int i = 0; i < EPL / 2; ++i) o[h][i] = make_float2(o[h][i].x * al.x, o[h][i].y * al.y);
+      m[h] = mn;
+      // p, duplicated as a pair, for the broadcast reads of p.V
+      *reinterpret_cast<float2*>(smem + C::kUOff + (warp * 32 + lane) * G * 8 + h * 8) = make_float2(pr, pr);
+    }
+    __syncwarp();
+    // ---- p.V, lane = output slice
+    const uint32_t vbase = vst + e_nb * C::kBT * 128 + (32 * warp) * 128;
+    if (nv == 32)
+      pv_rows<C, true>(vbase, voff, pbase, 32, o);
+    else
+      pv_rows<C, false>(vbase, voff, pbase, nv, o);
+    __syncwarp();
+  }
+
+  // Warp state -> merge slot `warp`: O[h][:] (unnormalised, on m[h]), m[h], l[h].
+  __device__ __forceinline__ void publish(float* obuf, float* mlbuf) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float lw = warp_sum(l[h]);
+      float* dst = obuf + (warp * G + h) * D + lane * EPL;
+#pragma unroll
+      for (int i = 0; i < EPL / 2; ++i) reinterpret_cast<float2*>(dst)[i] = o[h][i];
+      if (lane == 0) {
+        mlbuf[(warp * G + h) * 2] = m[h];
+        mlbuf[(warp * G + h) * 2 + 1] = lw;
+      }
+    }
+  }
+};
+
+template <class C, class E>
 __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTiles& tl, int64_t total,
                                                uint8_t* smem, volatile int* abort_flag) {
-  constexpr int G = C::G, D = C::D, W = C::kWarps, EPL = C::kEPL;
+  constexpr int G = C::G, D = C::D, W = C::kWarps;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
   constexpr int kCons = W * 32;
@@ -381,7 +516,6 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
   float* fin = reinterpret_cast<float*>(smem + C::kFinOff);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::kFlagOff + 4);
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t pbase = sbase + C::kUOff + warp * 32 * G * 8;
   const bool balanced = p.n_splits == 0;
   const bool fused = p.counters != nullptr;
 
@@ -401,17 +535,8 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
     }
   }
 
-  // Per-lane constants of the swizzled addressing.
-  const uint32_t xr = lane & 7;
-  // p.V: this lane's slice of a row
-  const int e_byte = lane * EPL * C::kEs;     // byte offset in the row
-  const int e_nb = e_byte / 128;               // column block
-  const int e_chunk = (e_byte % 128) / 16;     // 16-byte chunk within the block
-  const int e_in = e_byte % 16;                // byte within the chunk
-  uint32_t voff[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) voff[j] = ((e_chunk ^ j) << 4) + e_in;
-
+  E eng;
+  eng.setup(warp, lane, smem);
   uint32_t it = 0, qi = 0;
   bool ok = true;
 
@@ -419,15 +544,7 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
     int32_t head0, nh;
     vkv_heads(gr, pc.vkv, &head0, &nh);
     const bool nonempty = pc.tok_end > pc.tok_begin;
-    float m[G], l[G];
-    float2 o[G][EPL / 2];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.f;
-#pragma unroll
-      for (int i = 0; i < EPL / 2; ++i) o[h][i] = make_float2(0.f, 0.f);
-    }
+    eng.reset();
     const uint32_t qslot = qi & 1;
     if (nonempty && ok) {
       if (!mbar_wait(qfull + qslot, (qi >> 1) & 1)) {
@@ -435,6 +552,7 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
         *abort_flag = 1;
       }
       const uint32_t qaddr = sbase + C::kQOff + qslot * C::kQBytes;
+      if (ok) eng.begin(qaddr, p.qk_scale);
       for (int32_t t0 = pc.tok_begin; ok && t0 < pc.tok_end; t0 += C::kBT, ++it) {
         const uint32_t stage = it % C::kStages;
         if (*abort_flag || !mbar_wait(full + stage, (it / C::kStages) & 1)) {
@@ -447,97 +565,17 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
         nv = nv < 0 ? 0 : (nv > 32 ? 32 : nv);
         if (nv > 0) {
           const uint32_t kst = sbase + stage * C::kStageBytes;
-          const uint32_t vst = kst + C::kTileBytes;
-          // ---- q.k, lane = row
-          float2 acc[G][C::kAcc];
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int a = 0; a < C::kAcc; ++a) acc[h][a] = make_float2(0.f, 0.f);
-          const uint32_t krow = kst + (32 * warp + lane) * 128;
-#pragma unroll
-          for (int nb = 0; nb < C::kNB; ++nb) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int a = (nb * 8 + c) % C::kAcc;
-              const uint4 kw = lds128u(krow + nb * C::kBT * 128 + ((c ^ xr) << 4));
-              const int d0 = nb * (128 / C::kEs) + c * C::kChunkElems;
-              if constexpr (C::kBf16) {
-                const float2 k01 = make_float2(bf16_lo(kw.x), bf16_hi(kw.x));
-                const float2 k23 = make_float2(bf16_lo(kw.y), bf16_hi(kw.y));
-                const float2 k45 = make_float2(bf16_lo(kw.z), bf16_hi(kw.z));
-                const float2 k67 = make_float2(bf16_lo(kw.w), bf16_hi(kw.w));
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                  const float4 qa = lds128(qaddr + (h * D + d0) * 4);
-                  const float4 qb = lds128(qaddr + (h * D + d0 + 4) * 4);
-                  acc[h][a] = fma2(k01, make_float2(qa.x, qa.y), acc[h][a]);
-                  acc[h][a] = fma2(k23, make_float2(qa.z, qa.w), acc[h][a]);
-                  acc[h][a] = fma2(k45, make_float2(qb.x, qb.y), acc[h][a]);
-                  acc[h][a] = fma2(k67, make_float2(qb.z, qb.w), acc[h][a]);
-                }
-              } else {
-                const float2 k01 = make_float2(__uint_as_float(kw.x), __uint_as_float(kw.y));
-                const float2 k23 = make_float2(__uint_as_float(kw.z), __uint_as_float(kw.w));
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                  const float4 qa = lds128(qaddr + (h * D + d0) * 4);
-                  acc[h][a] = fma2(k01, make_float2(qa.x, qa.y), acc[h][a]);
-                  acc[h][a] = fma2(k23, make_float2(qa.z, qa.w), acc[h][a]);
-                }
-              }
-            }
-          }
-          // ---- online softmax over this warp's rows
-          const bool valid = lane < nv;
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float s = 0.f;
-#pragma unroll
-            for (int a = 0; a < C::kAcc; ++a) s += acc[h][a].x + acc[h][a].y;
-            s = valid ? s * p.qk_scale : -INFINITY;
-            const float mn = fmaxf(m[h], warp_max(s));
-            const float alpha = exp2f(m[h] - mn);
-            const float pr = exp2f(s - mn);
-            l[h] = fmaf(l[h], alpha, pr);
-            const float2 al = make_float2(alpha, alpha);
-#pragma unroll
-            for (int i = 0; i < EPL / 2; ++i) o[h][i] = make_float2(o[h][i].x * al.x, o[h][i].y * al.y);
-            m[h] = mn;
-            // p, duplicated as a pair, for the broadcast reads of p.V
-            *reinterpret_cast<float2*>(smem + C::kUOff + (warp * 32 + lane) * G * 8 + h * 8) =
-                make_float2(pr, pr);
-          }
-          __syncwarp();
-          // ---- p.V, lane = output slice
-          const uint32_t vbase = vst + e_nb * C::kBT * 128 + (32 * warp) * 128;
-          if (nv == 32)
-            pv_rows<C, true>(vbase, voff, pbase, 32, o);
-          else
-            pv_rows<C, false>(vbase, voff, pbase, nv, o);
-          __syncwarp();
+          eng.tile(kst, kst + C::kTileBytes, nv, qaddr, p.qk_scale);
         }
         if (lane == 0) mbar_arrive(empty + stage);
       }
     }
 
     // ---- merge the W warp states of this piece
-    float lw[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) lw[h] = warp_sum(l[h]);
-    named_barrier(1, kCons);  // every warp is past its last p.V: the p buffers may be reused
+    named_barrier(1, kCons);  // every warp is past its last tile: the p buffers may be reused
     if (nonempty && tid == 0) mbar_arrive(qempty + qslot);
     if (nonempty) ++qi;
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float* dst = obuf + (warp * G + h) * D + lane * EPL;
-#pragma unroll
-      for (int i = 0; i < EPL / 2; ++i) reinterpret_cast<float2*>(dst)[i] = o[h][i];
-      if (lane == 0) {
-        mlbuf[(warp * G + h) * 2] = m[h];
-        mlbuf[(warp * G + h) * 2 + 1] = lw[h];
-      }
-    }
+    eng.publish(obuf, mlbuf);
     named_barrier(1, kCons);
     if (tid < G) {
       float M = -INFINITY;
@@ -641,6 +679,12 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
   }
 }
 
+}  // namespace fdk
+
+#include "fd_split_mma.cuh"
+
+namespace fdk {
+
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fd_split_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -711,8 +755,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
   if (warp == C::kWarps)
     producer_warp<C>(&tmap_k, &tmap_v, p, tl, total, smem, abort_flag);
+  else if constexpr (C::kMma)
+    consumer_warps<C, MmaEngine<C>>(p, tl, total, smem, abort_flag);
   else
-    consumer_warps<C>(p, tl, total, smem, abort_flag);
+    consumer_warps<C, CoreEngine<C>>(p, tl, total, smem, abort_flag);
 }
 
 }  // namespace fdk

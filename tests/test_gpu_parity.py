@@ -66,6 +66,8 @@ SMALL = [
                lengths="uniform:1:500"),
     small_spec("paged64_gqa8", 2, 16, 2, 128, 700, layout="paged", page_size=64, lengths="uniform:1:700"),
     small_spec("peaked_q", 1, 4, 4, 128, 900, q_gain=6.0),
+    small_spec("peaked_q_gqa8", 2, 16, 2, 128, 900, q_gain=6.0, lengths="uniform:1:900"),
+    small_spec("gqa8_bf16_d64_ragged", 3, 16, 2, 64, 777, lengths="uniform:1:777"),
 ]
 
 
@@ -86,8 +88,9 @@ EDGE_LENGTHS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 127, 128, 129, 255, 256, 257, 1
 
 @pytest.mark.parametrize("layout,page", [("contiguous", 16), ("paged", 16), ("paged", 48)])
 @pytest.mark.parametrize("n_splits", [0, 2, 5])
-def test_edge_lengths(layout, page, n_splits):
-    spec = small_spec(f"edges_{layout}{page}", len(EDGE_LENGTHS), 8, 2, 128, 1024, layout=layout, page_size=page,
+@pytest.mark.parametrize("hq", [8, 16])  # GQA groups of 4 (CUDA-core engine) and 8 (tensor-core engine)
+def test_edge_lengths(layout, page, n_splits, hq):
+    spec = small_spec(f"edges_{layout}{page}", len(EDGE_LENGTHS), hq, 2, 128, 1024, layout=layout, page_size=page,
                       seed=11)
     case = make_case(spec, "cuda", lengths=EDGE_LENGTHS)
     ref_out, ref_lse = oracle_for(case)
@@ -146,8 +149,9 @@ def test_config5_paged_sampled():
 
 @pytest.mark.parametrize("layout", ["contiguous", "paged"])
 @pytest.mark.parametrize("n_splits", [0, 3])
-def test_masked_positions_are_bit_exact(layout, n_splits):
-    spec = small_spec(f"mask_{layout}", 6, 8, 2, 128, 700, layout=layout, lengths="uniform:1:700", seed=21)
+@pytest.mark.parametrize("hq,d", [(8, 128), (16, 128), (16, 64)])
+def test_masked_positions_are_bit_exact(layout, n_splits, hq, d):
+    spec = small_spec(f"mask_{layout}", 6, hq, 2, d, 700, layout=layout, lengths="uniform:1:700", seed=21)
     case = make_case(spec, "cuda")
     clean_out, clean_lse = run(case, n_splits=n_splits)
     for value in (float("nan"), float("inf"), -float("inf")):
