@@ -83,12 +83,16 @@ struct SplitCfg {
   static constexpr int kStages = kStagesFit > 4 ? 4 : kStagesFit;
   static constexpr int kEPL = D / 32;          // output elements per lane in p.V
   static constexpr int kChunkElems = 16 / kEs; // elements per 16-byte chunk
+  static constexpr int kChunks = kRowBytes / 16; // 16-byte chunks per row
   // Independent q.k accumulator chains per head: eight chains in all keep the
   // packed FMAs of one lane from waiting on each other.
   static constexpr int kAcc = G >= 8 ? 1 : 8 / G;
   static constexpr int kBoxBytes = 16 * 128;
-  // bf16 caches with eight query heads per CTA run q.k and p.V on mma.sync
-  static constexpr bool kMma = kBf16 && G == 8;
+
+  // bf16 caches with four or eight query heads per CTA run q.k and p.V on
+  // mma.sync; there the CUDA-core FMAs (and bf16 widening) bound the kernel
+  // well above its streaming time, while one or two heads per CTA stay cheap.
+  static constexpr bool kMma = kBf16 && G >= 4;
   static_assert(kNB >= 1 && kStages >= 2, "unsupported row size");
 
   // shared-memory layout (byte offsets from a 1024-aligned base)
@@ -191,18 +195,34 @@ __device__ __forceinline__ void merge_head(const float* o, const float* m, const
   if (lse_slot && lane == 0) *lse_slot = mx + logf(L);
 }
 
-// Calls f(piece) for every piece of this CTA, in the same order for every role.
-template <class F>
-__device__ __forceinline__ void for_each_piece(const SplitParams& p, const CtaTiles& tl, int64_t total,
-                                               F&& f) {
-  if (p.n_splits == 0) {
-    const int32_t grid = balanced_ctas(total, (int32_t)gridDim.x);
-    if ((int32_t)blockIdx.x >= grid) return;
-    BalancedWalk<CtaTiles> w(tl, p.B, p.hv, total, grid, (int32_t)blockIdx.x);
-    while (!w.done()) f(w.next());
-  } else {
+// The pieces of this CTA, in the same order for every role.
+struct PieceIter {
+  BalancedWalk<CtaTiles> walk;
+  const SplitParams& p;
+  bool balanced, pending;
+
+  __device__ __forceinline__ static int32_t walk_grid(const SplitParams& p, int64_t total) {
+    const int32_t g = p.n_splits == 0 ? balanced_ctas(total, (int32_t)gridDim.x) : 0;
+    return g > 0 ? g : 1;
+  }
+  __device__ __forceinline__ static bool walk_active(const SplitParams& p, int64_t total) {
+    return p.n_splits == 0 && total > 0 && (int32_t)blockIdx.x < balanced_ctas(total, (int32_t)gridDim.x);
+  }
+
+  __device__ __forceinline__ PieceIter(const SplitParams& p_, const CtaTiles& tl, int64_t total)
+      : walk(tl, p_.B, p_.hv, walk_active(p_, total) ? total : 0, walk_grid(p_, total),
+             walk_active(p_, total) ? (int32_t)blockIdx.x : 0),
+        p(p_), balanced(p_.n_splits == 0), pending(p_.n_splits != 0) {}
+
+  __device__ __forceinline__ bool next(Piece& pc) {
+    if (balanced) {
+      if (walk.done()) return false;
+      pc = walk.next();
+      return true;
+    }
+    if (!pending) return false;
+    pending = false;
     const int32_t pair = blockIdx.x, s = blockIdx.y;
-    Piece pc;
     pc.b = pair / p.hv;
     pc.vkv = pair % p.hv;
     const int32_t L = p.seq_lens ? clamp_len(__ldg(p.seq_lens + pc.b), p.max_len) : p.max_len;
@@ -211,9 +231,9 @@ __device__ __forceinline__ void for_each_piece(const SplitParams& p, const CtaTi
     pc.tok_begin = (int32_t)(lo < L ? lo : L);
     pc.tok_end = (int32_t)(hi > pc.tok_begin ? hi : pc.tok_begin);
     pc.slot = s;
-    f(pc);
+    return true;
   }
-}
+};
 
 // ----------------------------------------------------------------- producer
 template <class C>
@@ -233,8 +253,11 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
   gr.nsub = p.nsub;
   gr.hv = p.hv;
 
-  for_each_piece(p, tl, total, [&](const Piece& pc) {
-    if (!ok || pc.tok_end <= pc.tok_begin) return;
+  PieceIter pieces(p, tl, total);
+  Piece pc;
+  while (pieces.next(pc)) {
+    if (!ok) break;
+    if (pc.tok_end <= pc.tok_begin) continue;
     int32_t head0, nh;
     vkv_heads(gr, pc.vkv, &head0, &nh);
     const int32_t kvh = kv_head_of_vkv(gr, pc.vkv);
@@ -294,7 +317,7 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
         }
       }
     }
-  });
+  }
   if (!ok) {
     raise_error(p.err, kErrTimeout);
     *abort_flag = 1;
@@ -311,9 +334,10 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
 // ----------------------------------------------------------------- consumers
 // Each consumer warp owns key rows [32w, 32w+32) of every stage and keeps its
 // own running (m, l, O) per head.  Two engines compute a tile: the CUDA-core
-// engine below, and MmaEngine (fd_split_mma.cuh) for bf16 caches with eight
-// query heads per CTA, where q.k and p.V run on mma.sync.  Both publish the
-// warp state the same way, so the merge code is shared.
+// engine below (one or two heads per CTA, and fp32 caches), and MmaEngine
+// (fd_split_mma.cuh) for bf16 caches with four or eight query heads per CTA,
+// where q.k and p.V run on mma.sync.  Both publish the warp state the same
+// way, so the merge code is shared.
 
 template <class C, bool kFull>
 __device__ __forceinline__ void pv_rows(uint32_t vbase, const uint32_t* voff, uint32_t pbase, int nv,
@@ -540,7 +564,9 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
   uint32_t it = 0, qi = 0;
   bool ok = true;
 
-  for_each_piece(p, tl, total, [&](const Piece& pc) {
+  PieceIter pieces(p, tl, total);
+  Piece pc;
+  while (pieces.next(pc)) {
     int32_t head0, nh;
     vkv_heads(gr, pc.vkv, &head0, &nh);
     const bool nonempty = pc.tok_end > pc.tok_begin;
@@ -672,7 +698,7 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
       }
     }
     named_barrier(1, kCons);  // shared merge buffers are free again
-  });
+  }
   if (!ok) {
     raise_error(p.err, kErrTimeout);
     *abort_flag = 1;

@@ -1,13 +1,14 @@
 // fd_split_mma.cuh -- tensor-core tile engine of the split kernel, for bf16
-// K/V caches with eight query heads per CTA (GQA groups of 8, or larger groups
-// taken eight heads at a time).
+// K/V caches with four or eight query heads per CTA (GQA groups of 4 or 8, or
+// larger groups taken eight heads at a time).
 //
-// With g = 8 every key costs 4*D*8 flops against 4*D bytes of K and V; on CUDA
-// cores the q.k and p.V FMAs then bound the kernel well below the memory roof.
-// Here one warp handles its 32 keys of a stage with mma.sync m16n8k16 (bf16 in,
-// fp32 accumulate):
+// With g heads per KV head every key costs 4*D*g flops against 4*D bytes of K
+// and V, plus the widening of every bf16 element; on CUDA cores, from g = 4 on,
+// that arithmetic keeps the kernel well above the time the TMA stream alone
+// takes.  Here one warp handles its 32 keys of a stage with mma.sync m16n8k16
+// (bf16 in, fp32 accumulate), heads on the M axis (rows >= g are idle):
 //
-//   q.k:  A = the eight heads' q rows, split into bf16 hi (rows 0-7) and lo
+//   q.k:  A = the g heads' q rows, split into bf16 hi (rows 0-7) and lo
 //         (rows 8-15) parts with q = hi + lo to ~2^-16; B = K^T straight from the
 //         swizzled stage via ldmatrix.  One MMA yields q_hi.k and q_lo.k in the
 //         same thread (C rows g and g+8), whose sum is q.k to fp32 accuracy.
@@ -74,7 +75,8 @@ struct MmaEngine {
   static constexpr int NT = D / 8;   // n-tiles of p.V
   static constexpr int kRowStride = 128;
   static constexpr int kBlk = C::kBT * 128;  // bytes of one 128-byte column block of a stage tile
-  static_assert(C::G == 8 && C::kBf16 && C::kBT == 128 && C::kWarps == 4, "MMA engine layout");
+  static constexpr int G = C::G;
+  static_assert((G == 4 || G == 8) && C::kBf16 && C::kBT == 128 && C::kWarps == 4, "MMA engine layout");
 
   uint32_t qa[KS][4];  // A fragments of q (hi rows 0-7, lo rows 8-15) for each k-step
   float o[NT][4];      // p.V accumulators: [.][0..1] from p_hi, [.][2..3] from p_lo
@@ -125,8 +127,11 @@ struct MmaEngine {
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
       const uint32_t a = qaddr + (g * D + 16 * kk + 2 * t) * 4;
-      const float2 x0 = lds64f(a);       // d, d+1
-      const float2 x1 = lds64f(a + 32);  // d+8, d+9
+      float2 x0 = make_float2(0.f, 0.f), x1 = x0;  // rows of heads >= G stay zero
+      if (g < G) {
+        x0 = lds64f(a);       // d, d+1
+        x1 = lds64f(a + 32);  // d+8, d+9
+      }
       split_bf16x2(x0.x * qk_scale, x0.y * qk_scale, qa[kk][0], qa[kk][1]);
       split_bf16x2(x1.x * qk_scale, x1.y * qk_scale, qa[kk][2], qa[kk][3]);
     }
@@ -218,13 +223,14 @@ struct MmaEngine {
     const float f = m == -INFINITY ? 0.f : exp2f(m - mt);
     float ls = l + __shfl_xor_sync(0xffffffffu, l, 1);
     ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-    float* row = obuf + (warp * 8 + g) * D + 2 * t;
+    if (g >= G) return;  // idle rows
+    float* row = obuf + (warp * G + g) * D + 2 * t;
 #pragma unroll
     for (int n = 0; n < NT; ++n)
       *reinterpret_cast<float2*>(row + 8 * n) = make_float2((o[n][0] + o[n][2]) * f, (o[n][1] + o[n][3]) * f);
     if (t == 0) {
-      mlbuf[(warp * 8 + g) * 2] = mt;
-      mlbuf[(warp * 8 + g) * 2 + 1] = ls * f;
+      mlbuf[(warp * G + g) * 2] = mt;
+      mlbuf[(warp * G + g) * 2 + 1] = ls * f;
     }
   }
 };
