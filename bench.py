@@ -14,6 +14,7 @@ method has) on the host cores, on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import glob
 import hashlib
 import json
@@ -40,6 +41,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["fdecode", "reference"], default="fdecode")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the workload with this batch size instead of its own (smaller profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -298,6 +301,8 @@ def run_fdecode(args):
     fd.load_library()
 
     spec = CONFIGS[args.workload]
+    if args.batch > 0:
+        spec = dataclasses.replace(spec, B=args.batch, name=f"{spec.name}_batch{args.batch}")
     case = make_case(spec, device)
     step_bytes = workload_bytes(case)
     kv_bytes = case.kv_bytes()
