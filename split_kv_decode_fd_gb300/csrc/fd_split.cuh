@@ -138,60 +138,116 @@ struct CtaTiles {
 
 // Log-sum-exp merge of `count` split states of one head (the combine
 // walkthrough), by one warp.  Split k lives at o + (base + k*stride)*D and
-// m/l + base + k*stride.  Fixed summation order: bit-reproducible.
+// m/l + base + k*stride.  The loads are issued in batches so that the merge
+// costs a few L2 round trips rather than one per split.  Summation order is
+// fixed: per output element, four partial sums over k = 0, 1, 2, 3 (mod 4) in
+// increasing k, then ((s0 + s1) + s2) + s3 -- bit-reproducible, and the same
+// for the fused merge and fd_combine.
+template <int D>
+__device__ __forceinline__ void load_slice(const float* row, float (&v)[D / 32]) {
+  if constexpr (D / 32 == 4) {
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(row));
+    v[0] = x.x;
+    v[1] = x.y;
+    v[2] = x.z;
+    v[3] = x.w;
+  } else {
+    const float2 x = __ldcg(reinterpret_cast<const float2*>(row));
+    v[0] = x.x;
+    v[1] = x.y;
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void merge_head(const float* o, const float* m, const float* l, size_t base,
                                            size_t stride, int count, float* out_row, float* lse_slot,
                                            int lane) {
   constexpr int EPL = D / 32;
+  constexpr int KR = 4;                 // splits per lane whose (m, l) stay in registers: count <= 128
+  constexpr int NB = 128 / EPL;         // splits per batch of O loads (128 registers)
+  const float* src = o + base * D + lane * EPL;
+  // Round trip 1: every (m, l) and the first batch of O slices, all in flight together.
+  float mk[KR], lk[KR];
+#pragma unroll
+  for (int r = 0; r < KR; ++r) {
+    const int k = r * 32 + lane;
+    mk[r] = -INFINITY;
+    lk[r] = 0.f;
+    if (k < count) {
+      const size_t i = base + (size_t)k * stride;
+      lk[r] = __ldcg(l + i);
+      mk[r] = __ldcg(m + i);
+    }
+  }
+  float v[NB][EPL];
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) v[j][e] = 0.f;
+    if (j < count) load_slice<D>(src + (size_t)j * stride * D, v[j]);
+  }
   float mx = -INFINITY;
-  for (int k = lane; k < count; k += 32) {
+#pragma unroll
+  for (int r = 0; r < KR; ++r)
+    if (lk[r] > 0.f) mx = fmaxf(mx, mk[r]);
+  for (int k = KR * 32 + lane; k < count; k += 32) {
     const size_t i = base + (size_t)k * stride;
     if (__ldcg(l + i) > 0.f) mx = fmaxf(mx, __ldcg(m + i));
   }
   mx = warp_max(mx);
-  float acc[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
   if (mx == -INFINITY) {
 #pragma unroll
     for (int e = 0; e < EPL; ++e) out_row[lane * EPL + e] = 0.f;
     if (lse_slot && lane == 0) *lse_slot = -INFINITY;
     return;
   }
+  float wk[KR];
   float lsum = 0.f;
-  for (int k0 = 0; k0 < count; k0 += 32) {
-    const int k = k0 + lane;
-    float w = 0.f;
-    if (k < count) {
-      const size_t i = base + (size_t)k * stride;
-      const float lk = __ldcg(l + i);
-      if (lk > 0.f) {
-        w = exp2f((__ldcg(m + i) - mx) * kLog2e);
-        lsum = fmaf(w, lk, lsum);
-      }
-    }
-    const int n = count - k0 < 32 ? count - k0 : 32;
-    for (int j = 0; j < n; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, w, j);
-      if (wj == 0.f) continue;  // warp-uniform
-      const float* src = o + (base + (size_t)(k0 + j) * stride) * D + lane * EPL;
-      if constexpr (EPL == 4) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-        acc[0] = fmaf(wj, v.x, acc[0]);
-        acc[1] = fmaf(wj, v.y, acc[1]);
-        acc[2] = fmaf(wj, v.z, acc[2]);
-        acc[3] = fmaf(wj, v.w, acc[3]);
-      } else {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-        acc[0] = fmaf(wj, v.x, acc[0]);
-        acc[1] = fmaf(wj, v.y, acc[1]);
-      }
-    }
+#pragma unroll
+  for (int r = 0; r < KR; ++r) {
+    wk[r] = lk[r] > 0.f ? exp2f((mk[r] - mx) * kLog2e) : 0.f;
+    lsum = fmaf(wk[r], lk[r], lsum);
+  }
+  for (int k = KR * 32 + lane; k < count; k += 32) {
+    const size_t i = base + (size_t)k * stride;
+    const float lv = __ldcg(l + i);
+    if (lv > 0.f) lsum = fmaf(exp2f((__ldcg(m + i) - mx) * kLog2e), lv, lsum);
   }
   const float L = warp_sum(lsum);
+  float acc[4][EPL];
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) out_row[lane * EPL + e] = acc[e] / L;
+  for (int s4 = 0; s4 < 4; ++s4)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[s4][e] = 0.f;
+  for (int k0 = 0; k0 < count; k0 += NB) {
+    if (k0 > 0) {  // later batches
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) v[j][e] = 0.f;
+        if (k0 + j < count) load_slice<D>(src + (size_t)(k0 + j) * stride * D, v[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int k = k0 + j;
+      if (k >= count) break;  // warp-uniform
+      const int r = k >> 5;
+      float w;
+      if (r < KR) {
+        const float ws = r == 0 ? wk[0] : (r == 1 ? wk[1] : (r == 2 ? wk[2] : wk[3]));
+        w = __shfl_sync(0xffffffffu, ws, k & 31);
+      } else {
+        const size_t i = base + (size_t)k * stride;
+        const float lv = __ldcg(l + i);
+        w = lv > 0.f ? exp2f((__ldcg(m + i) - mx) * kLog2e) : 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[j & 3][e] = fmaf(w, v[j][e], acc[j & 3][e]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) out_row[lane * EPL + e] = (((acc[0][e] + acc[1][e]) + acc[2][e]) + acc[3][e]) / L;
   if (lse_slot && lane == 0) *lse_slot = mx + logf(L);
 }
 
@@ -668,12 +724,13 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
     }
 
     if (fused && !final_here) {
-      __threadfence();
+      // The barrier orders every thread's partial stores before thread 0's
+      // release; its acquire, then the barrier, orders the other pieces'
+      // partials before this CTA's reads if it arrives last.
       named_barrier(1, kCons);
-      if (tid == 0) *last_flag = (atomicAdd(p.counters + pair, 1) == npieces - 1) ? 1 : 0;
+      if (tid == 0) *last_flag = (atomic_add_acq_rel(p.counters + pair, 1) == npieces - 1) ? 1 : 0;
       named_barrier(1, kCons);
       if (*last_flag) {
-        __threadfence();
         size_t base0, stride;
         int count;
         if (balanced) {
