@@ -329,15 +329,22 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
     }
     ++qi;
     ok = __shfl_sync(0xffffffffu, ok, 0);
+    // Paged: lane j looks up the page of row block j of a tile one tile ahead, so
+    // the table load overlaps the wait for a free stage.  Only entries of keys
+    // below tok_end (<= L_b) are ever read.
+    const int32_t* trow = p.paged ? p.block_table + (size_t)pc.b * p.max_pages : nullptr;
+    int32_t page_next = 0;
+    if (p.paged && pc.tok_begin + 16 * lane < pc.tok_end)
+      page_next = __ldg(trow + (pc.tok_begin + 16 * lane) / p.page_size);
     for (int32_t t0 = pc.tok_begin; ok && t0 < pc.tok_end; t0 += C::kBT, ++it) {
       const int32_t nvalid = pc.tok_end - t0 < C::kBT ? pc.tok_end - t0 : C::kBT;
       const int32_t nbox = ceil_div(nvalid, 16);
-      int32_t page = 0;
+      int32_t page = page_next;
       bool mine = lane < nbox;
-      if (mine && p.paged) {
-        const int32_t tok = t0 + 16 * lane;
-        page = __ldg(p.block_table + (size_t)pc.b * p.max_pages + tok / p.page_size);
-        if (page < 0 || page >= p.num_pages) {
+      if (p.paged) {
+        const int32_t tn = t0 + C::kBT + 16 * lane;
+        if (tn < pc.tok_end) page_next = __ldg(trow + tn / p.page_size);
+        if (mine && (page < 0 || page >= p.num_pages)) {
           raise_error(p.err, kErrBadIndex);
           mine = false;
         }
