@@ -42,6 +42,10 @@ Readings taken where the pages are silent:
   ``t % page_size``.
 * Explicit split size: ``S = 16 * ceil(ceil(max_seq_len / n_splits) / 16)``;
   split ``s`` covers tokens ``[s*S, min((s+1)*S, L_b))``.
+* Several query rows per sequence ("FlashDecoding and split-KV": one query row,
+  or a small batch of them): the ``n_q`` new tokens are the last ``n_q`` keys of
+  the cache; with causal masking row ``i`` attends keys ``t < L_b - (n_q-1-i)``,
+  without it every row attends all ``L_b`` keys.
 
 All arithmetic is float64.  Inputs are widened exactly (bf16 and fp32 values are
 exactly representable in float64); ``scale`` is taken as given.
@@ -64,6 +68,8 @@ __all__ = [
     "decode",
     "explicit_split_size",
     "split_partials",
+    "row_key_limit",
+    "decode_rows",
 ]
 
 
@@ -263,3 +269,44 @@ def split_partials(q, k, v, scale, n_splits, seq_lens=None, max_seq_len=None,
                     o_part[b, h, s], m_part[b, h, s], l_part[b, h, s] = split_state(
                         q[b, h], k_rows[lo:hi], v_rows[lo:hi], scale)
     return o_part, m_part, l_part
+
+
+def row_key_limit(length: int, n_q: int, row: int, causal: bool) -> int:
+    """Number of keys row ``row`` of ``n_q`` query rows attends (never below 0).
+
+    Reading for a small batch of query rows per sequence: the rows are the last
+    ``n_q`` tokens, already written to the cache, so under causal masking row
+    ``i`` sees keys ``t < L_b - (n_q - 1 - i)``; otherwise all ``L_b`` keys.
+    """
+    lim = length - (n_q - 1 - row) if causal else length
+    return max(0, min(lim, length))
+
+
+def decode_rows(q, k, v, scale, causal=True, seq_lens=None, max_seq_len=None, block_table=None,
+                page_size=None):
+    """Decode attention with ``n_q`` query rows per (batch, head).
+
+    ``q``: ``[B, Hq, n_q, D]``; other arguments as in :func:`decode`.  Returns
+    ``(out [B, Hq, n_q, D], lse [B, Hq, n_q])``; a row with no keys gives zeros
+    and ``-inf``.
+    """
+    q = _f64(q)
+    batch, hq, n_q, d = q.shape
+    hkv = np.shape(k)[1]
+    g = hq // hkv
+    if block_table is None and max_seq_len is None:
+        max_seq_len = np.shape(k)[2]
+    lens = _lengths(seq_lens, batch, max_seq_len)
+    out = np.zeros((batch, hq, n_q, d), dtype=np.float64)
+    lse = np.full((batch, hq, n_q), -math.inf, dtype=np.float64)
+    for b in range(batch):
+        for kvh in range(hkv):
+            k_rows = sequence_rows(k, b, kvh, lens[b], block_table, page_size)
+            v_rows = sequence_rows(v, b, kvh, lens[b], block_table, page_size)
+            for h in range(hq):
+                if kv_head_for(h, g) != kvh:
+                    continue
+                for i in range(n_q):
+                    lim = row_key_limit(lens[b], n_q, i, causal)
+                    out[b, h, i], lse[b, h, i] = attend_row(q[b, h, i], k_rows[:lim], v_rows[:lim], scale)
+    return out, lse

@@ -339,6 +339,49 @@ def check_paged_matches_gather():
     assert np.array_equal(out_p2, out_p) and np.array_equal(lse_p2, lse_p)
 
 
+# ------------------------------------------------------------ several query rows
+def check_rows_against_sdpa_with_mask():
+    """Multi-row decode equals SDPA (float64) under the explicit per-row key mask."""
+    import torch
+    import torch.nn.functional as F
+    for causal in (True, False):
+        for Hq, Hkv, n_q in ((4, 4, 3), (8, 2, 2), (8, 1, 5)):
+            r = _rng(40 + Hq + n_q)
+            B, D, T = 2, 8, 23
+            q = r.standard_normal((B, Hq, n_q, D))
+            k = r.standard_normal((B, Hkv, T, D))
+            v = r.standard_normal((B, Hkv, T, D))
+            lens = [23, 9]
+            out, lse = oracle.decode_rows(q, k, v, 0.3, causal=causal, seq_lens=lens)
+            g = Hq // Hkv
+            for b in range(B):
+                L = lens[b]
+                kt = torch.from_numpy(k[b, :, :L][None]).repeat_interleave(g, dim=1)
+                vt = torch.from_numpy(v[b, :, :L][None]).repeat_interleave(g, dim=1)
+                mask = torch.ones(n_q, L, dtype=torch.bool)
+                if causal:  # row i sees keys t <= L - n_q + i
+                    mask = torch.arange(L)[None, :] <= (L - n_q + torch.arange(n_q))[:, None]
+                ref = F.scaled_dot_product_attention(torch.from_numpy(q[b][None]), kt, vt, attn_mask=mask,
+                                                     scale=0.3)[0].numpy()
+                np.testing.assert_allclose(out[b], ref, rtol=0, atol=1e-13)
+
+
+def check_rows_reduce_to_single_row():
+    """One query row (or the last causal row) is plain decode; rows past the keys are empty."""
+    q, k, v, lens = random_problem(41, B=2, Hq=4, Hkv=2, D=8, T=30)
+    lens = [30, 2]
+    o1, l1 = oracle.decode(q, k, v, 0.5, seq_lens=lens)
+    o2, l2 = oracle.decode_rows(q[:, :, None, :], k, v, 0.5, seq_lens=lens)
+    assert np.array_equal(o1, o2[:, :, 0]) and np.array_equal(l1, l2[:, :, 0])
+    q4 = _rng(42).standard_normal((2, 4, 4, 8))
+    o4, l4 = oracle.decode_rows(q4, k, v, 0.5, causal=True, seq_lens=lens)
+    ol, ll = oracle.decode(q4[:, :, -1], k, v, 0.5, seq_lens=lens)
+    assert np.array_equal(o4[:, :, -1], ol) and np.array_equal(l4[:, :, -1], ll)
+    # sequence 1 has 2 keys and 4 causal rows: rows 0 and 1 see no key
+    assert np.all(o4[1, :, :2] == 0) and np.all(np.isneginf(l4[1, :, :2]))
+    assert oracle.row_key_limit(2, 4, 2, True) == 1 and oracle.row_key_limit(2, 4, 0, False) == 2
+
+
 ALL_CHECKS = [
     check_single_key,
     check_identical_keys_mean,
@@ -353,6 +396,8 @@ ALL_CHECKS = [
     check_brute_force_mpmath,
     check_torch_sdpa,
     check_paged_matches_gather,
+    check_rows_against_sdpa_with_mask,
+    check_rows_reduce_to_single_row,
 ]
 
 

@@ -121,7 +121,13 @@ def _mut_transposed_v(q_row, k_rows, v_rows, scale):
     return (w @ np.asarray(k_rows, dtype=np.float64)) / w.sum(), m + math.log(w.sum())
 
 
+def _mut_row_limit_off_by_one(length, n_q, row, causal):
+    lim = length - (n_q - row) if causal else length  # one key short
+    return max(0, min(lim, length))
+
+
 MUTANTS = {
+    "row_limit_off_by_one": {"row_key_limit": _mut_row_limit_off_by_one},
     "head_map_modulo": {"kv_head_for": _mut_head_map},
     "scale_dropped": {"scores": _mut_no_scale},
     "lse_without_max": {"attend_row": _mut_lse_without_max},
