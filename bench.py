@@ -43,6 +43,8 @@ def parse_args():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--batch", type=int, default=0,
                     help="run the workload with this batch size instead of its own (smaller profiling captures)")
+    ap.add_argument("--rows", type=int, default=1,
+                    help="query rows per sequence (causal window through fd_decode_rows); 1 = fd_decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -303,18 +305,30 @@ def run_fdecode(args):
     spec = CONFIGS[args.workload]
     if args.batch > 0:
         spec = dataclasses.replace(spec, B=args.batch, name=f"{spec.name}_batch{args.batch}")
+    n_q = args.rows
+    if n_q > 1:
+        spec = dataclasses.replace(spec, name=f"{spec.name}_rows{n_q}_causal")
     case = make_case(spec, device)
-    step_bytes = workload_bytes(case)
     kv_bytes = case.kv_bytes()
-    out = torch.empty((spec.B, spec.Hq, spec.D), dtype=torch.float32, device=device)
-    lse = torch.empty((spec.B, spec.Hq), dtype=torch.float32, device=device)
+    step_bytes = kv_bytes + spec.B * spec.Hq * n_q * spec.D * 4 * 2
+    rows_shape = (spec.B, spec.Hq, n_q) if n_q > 1 else (spec.B, spec.Hq)
+    out = torch.empty(rows_shape + (spec.D,), dtype=torch.float32, device=device)
+    lse = torch.empty(rows_shape, dtype=torch.float32, device=device)
     ws = fd.Workspace()
     stream = torch.cuda.current_stream(device)
+    if n_q > 1:
+        gen = torch.Generator(device=device).manual_seed(spec.seed + 17)
+        q_rows = torch.randn(rows_shape + (spec.D,), generator=gen, device=device, dtype=torch.float32)
 
-    def step():
-        fd.decode(case.q, case.k, case.v, seq_lens=case.seq_lens, max_seq_len=case.max_seq_len,
-                  block_table=case.block_table, scale=spec.scale, n_splits=spec.n_splits, out=out, lse=lse,
-                  workspace=ws)
+        def step():
+            fd.decode_rows(q_rows, case.k, case.v, causal=True, seq_lens=case.seq_lens,
+                           max_seq_len=case.max_seq_len, block_table=case.block_table, scale=spec.scale,
+                           n_splits=spec.n_splits, out=out, lse=lse, workspace=ws)
+    else:
+        def step():
+            fd.decode(case.q, case.k, case.v, seq_lens=case.seq_lens, max_seq_len=case.max_seq_len,
+                      block_table=case.block_table, scale=spec.scale, n_splits=spec.n_splits, out=out, lse=lse,
+                      workspace=ws)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -351,17 +365,35 @@ def run_fdecode(args):
     achieved = step_bytes / (mean_launch_us * 1e-6) / 1e9
     peak, peak_src = measured_peak()
 
-    # ---- end to end: host q in, host out/lse back, through fd_decode_host
-    q_host = case.q.cpu().pin_memory()
+    # ---- end to end: host q in, host out/lse back (fd_decode_host; with rows, copies around fd_decode_rows)
+    q_host = (q_rows if n_q > 1 else case.q).cpu().pin_memory()
     lens_host = None if case.seq_lens is None else case.seq_lens.cpu()
-    out_h = torch.empty((spec.B, spec.Hq, spec.D), dtype=torch.float32, pin_memory=True)
-    lse_h = torch.empty((spec.B, spec.Hq), dtype=torch.float32, pin_memory=True)
+    out_h = torch.empty(rows_shape + (spec.D,), dtype=torch.float32, pin_memory=True)
+    lse_h = torch.empty(rows_shape, dtype=torch.float32, pin_memory=True)
     ws_h = fd.Workspace()
+    e2e_api = "fd_decode_host"
+    if n_q > 1:
+        e2e_api = "pinned copies + fd_decode_rows"
+        q_dev = torch.empty_like(q_rows)
+        lens_dev = None if lens_host is None else torch.empty_like(case.seq_lens)
+        lens_pinned = None if lens_host is None else lens_host.pin_memory()
+        out_d, lse_d = torch.empty_like(out), torch.empty_like(lse)
 
-    def e2e_step():
-        fd.decode_host(q_host, case.k, case.v, seq_lens_host=lens_host, max_seq_len=case.max_seq_len,
-                       block_table=case.block_table, scale=spec.scale, n_splits=spec.n_splits, out_host=out_h,
-                       lse_host=lse_h, workspace=ws_h)
+        def e2e_step():
+            q_dev.copy_(q_host, non_blocking=True)
+            if lens_dev is not None:
+                lens_dev.copy_(lens_pinned, non_blocking=True)
+            fd.decode_rows(q_dev, case.k, case.v, causal=True, seq_lens=lens_dev, max_seq_len=case.max_seq_len,
+                           block_table=case.block_table, scale=spec.scale, n_splits=spec.n_splits, out=out_d,
+                           lse=lse_d, workspace=ws_h)
+            out_h.copy_(out_d, non_blocking=True)
+            lse_h.copy_(lse_d, non_blocking=True)
+            torch.cuda.current_stream(device).synchronize()
+    else:
+        def e2e_step():
+            fd.decode_host(q_host, case.k, case.v, seq_lens_host=lens_host, max_seq_len=case.max_seq_len,
+                           block_table=case.block_table, scale=spec.scale, n_splits=spec.n_splits,
+                           out_host=out_h, lse_host=lse_h, workspace=ws_h)
 
     for _ in range(max(3, args.warmup)):
         e2e_step()
@@ -383,13 +415,13 @@ def run_fdecode(args):
         return 0
     # ---- CPU baseline: the oracle on a bounded sample, host cores, rank 0 at N=1
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and n_q == 1:
         v, note, el = OracleSampler(case).whole_groups(args.cpu_seconds)
         cpu = {"value": v, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle", "sample": note,
                "seconds": round(el, 2)}
 
     gpd = fd.workspace_status(ws)
-    g = spec.Hq // spec.Hkv
+    g = spec.Hq * n_q // spec.Hkv
     gpad = 1
     while gpad < g and gpad < 8:
         gpad *= 2
@@ -400,6 +432,7 @@ def run_fdecode(args):
         "data": "synthetic",
         "config": {"workload": spec.name, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "D": spec.D,
                    "T": spec.T_cap, "kv_dtype": spec.kv_dtype, "q_dtype": "f32", "layout": spec.layout,
+                   "rows": n_q,
                    "kv_bytes_per_step": kv_bytes, "bytes_per_step": step_bytes,
                    "l2": f"inputs {kv_bytes / 1e6:.0f} MB > 129 MB L2; no flush",
                    "plan": "balanced" if spec.n_splits == 0 else f"n_splits={spec.n_splits}",
@@ -411,7 +444,7 @@ def run_fdecode(args):
                      "peak_source": peak_src, "kernel": "fd_split_kernel", "launches_per_step": 1,
                      "mean_launch_us": mean_launch_us},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": k_e2e, "api": "fd_decode_host"},
+                "steps": k_e2e, "api": e2e_api},
         "gpu_launches": K,
         "clocks": clocks,
         "cpu_baseline": cpu,

@@ -157,6 +157,23 @@ FD_API fd_status fd_decode(const float* q, const fd_kv_desc* kv, float* out, flo
                     void* stream);
 
 /*
+ * Decode with n_q query rows per (batch, head) sharing one read of K/V, for a
+ * small batch of new tokens per sequence (e.g. verifying speculative tokens;
+ * "FlashDecoding and split-KV" names one query row or a small batch of them).
+ *   q    [B, Hq, n_q, D] fp32; out [B, Hq, n_q, D]; lse [B, Hq, n_q] or NULL.
+ *   causal = 1: the n_q rows are the last n_q tokens, already in the cache, and
+ *            row i attends keys t < L_b - (n_q - 1 - i); causal = 0: every row
+ *            attends all L_b keys.  A row with no key gives out = 0, lse = -inf.
+ *   1 <= n_q <= 64.  Other arguments as in fd_decode; the workspace is
+ *   fd_workspace_bytes(B, Hq * n_q, Hkv, D, n_splits, 0).  The rows of a GQA
+ *   group are served together (up to 8 rows x heads per K/V read).
+ */
+FD_API fd_status fd_decode_rows(const float* q, int32_t n_q, int32_t causal, const fd_kv_desc* kv, float* out,
+                                float* lse, int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_lens,
+                                int32_t max_seq_len, int32_t D, float scale, int32_t n_splits, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
  * Split step only ("fd_split" of the walkthrough), with n_splits > 0 splits
  * per sequence of fd_split_size(max_seq_len, n_splits) tokens each.  Writes:
  *   o_part [B, Hq, n_splits, D]  unnormalised sum_t exp(s_t - m_s) v_t

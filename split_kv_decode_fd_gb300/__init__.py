@@ -13,6 +13,7 @@ from .fdecode import (  # noqa: F401
     combine,
     decode,
     decode_host,
+    decode_rows,
     decode_static,
     library_path,
     load_library,

@@ -185,6 +185,8 @@ SplitParams base_params(const float* q, const fd_kv_desc* kv, int B, int Hq, int
   p.max_pages = kv->max_pages_per_seq;
   p.num_pages = kv->num_pages;
   p.qk_scale = (float)((double)scale * 1.4426950408889634);
+  p.n_q = 1;
+  p.causal = 0;
   return p;
 }
 
@@ -272,9 +274,15 @@ fd_status fd_workspace_status(void* workspace, size_t workspace_bytes, void* str
   return FD_ERR_BAD_INDEX;
 }
 
-fd_status fd_decode(const float* q, const fd_kv_desc* kv, float* out, float* lse, int32_t B, int32_t Hq,
-                    int32_t Hkv, const int32_t* seq_lens, int32_t max_seq_len, int32_t D, float scale,
-                    int32_t n_splits, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// fd_decode over Hq "virtual heads" = query heads x rows (n_q rows per head).
+fd_status decode_impl(const float* q, const fd_kv_desc* kv, float* out, float* lse, int32_t B, int32_t Hq,
+                      int32_t Hkv, const int32_t* seq_lens, int32_t max_seq_len, int32_t D, float scale,
+                      int32_t n_splits, void* workspace, size_t workspace_bytes, void* stream, int32_t n_q,
+                      int32_t causal) {
   fd_status st = check_shape(B, Hq, Hkv, D);
   if (st != FD_OK) return st;
   if (!q || !out || !workspace || !aligned16(q) || !aligned16(out) || !aligned16(workspace))
@@ -293,6 +301,8 @@ fd_status fd_decode(const float* q, const fd_kv_desc* kv, float* out, float* lse
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   SplitParams p = base_params(q, kv, B, Hq, Hkv, seq_lens, max_seq_len, scale);
+  p.n_q = n_q;
+  p.causal = causal;
   p.out = out;
   p.lse = lse;
   p.o_part = reinterpret_cast<float*>(ws + w.o);
@@ -317,6 +327,27 @@ fd_status fd_decode(const float* q, const fd_kv_desc* kv, float* out, float* lse
   if ((st = launch(kv, D, p, grid, s)) != FD_OK) return st;
   const cudaError_t e = launch_combine(D, p.o_part, p.m_part, p.l_part, out, lse, B * Hq, n_splits, s);
   return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fd_status fd_decode(const float* q, const fd_kv_desc* kv, float* out, float* lse, int32_t B, int32_t Hq,
+                    int32_t Hkv, const int32_t* seq_lens, int32_t max_seq_len, int32_t D, float scale,
+                    int32_t n_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(q, kv, out, lse, B, Hq, Hkv, seq_lens, max_seq_len, D, scale, n_splits, workspace,
+                     workspace_bytes, stream, 1, 0);
+}
+
+fd_status fd_decode_rows(const float* q, int32_t n_q, int32_t causal, const fd_kv_desc* kv, float* out,
+                         float* lse, int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_lens,
+                         int32_t max_seq_len, int32_t D, float scale, int32_t n_splits, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (n_q < 1 || n_q > 64 || (causal != 0 && causal != 1)) return FD_ERR_INVALID_ARG;
+  if (Hq < 1 || (int64_t)Hq * n_q > ((int64_t)1 << 24)) return FD_ERR_INVALID_ARG;
+  return decode_impl(q, kv, out, lse, B, Hq * n_q, Hkv, seq_lens, max_seq_len, D, scale, n_splits, workspace,
+                     workspace_bytes, stream, n_q, causal);
 }
 
 fd_status fd_split_partial(const float* q, const fd_kv_desc* kv, int32_t B, int32_t Hq, int32_t Hkv,
@@ -433,6 +464,7 @@ int64_t fd_plan_pieces(int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_le
         pc.tok_begin = (int32_t)std::min<int64_t>(lo, L);
         pc.tok_end = (int32_t)std::max<int64_t>(hi, pc.tok_begin);
         pc.slot = s;
+        pc.len = (int32_t)L;
         emit(pair * n_splits + s, pc, n_splits);
       }
     }

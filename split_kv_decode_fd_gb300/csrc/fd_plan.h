@@ -107,6 +107,7 @@ struct Piece {
   int32_t b, vkv;
   int32_t tok_begin, tok_end;  // keys [tok_begin, tok_end), already clipped to L_b
   int32_t slot;                // balanced: output slot; explicit: split index
+  int32_t len;                 // L_b, the valid length of sequence b
 };
 
 // Walk of one CTA over its tile range in the balanced plan.  `Tiles` maps a
@@ -156,6 +157,7 @@ struct BalancedWalk {
     int32_t e = (tile + take) * kPlanTile;
     int32_t L = tl.len(b);
     pc.tok_end = e < L ? e : L;
+    pc.len = L;
     pc.slot = (b * hv + vkv) + cta;
     flat += take;
     tile += take;

@@ -64,6 +64,20 @@ struct SplitParams {
   int32_t paged;
   int32_t page_size, max_pages, num_pages;
   float qk_scale;          // scale * log2(e)
+  int32_t n_q;             // query rows per (b, head): virtual head h' = head * n_q + row
+  int32_t causal;          // rows see keys t < L_b - (n_q - 1 - row) (else all L_b keys)
+};
+
+// Keys seen by the heads of one piece: head0 + j for j < nh; virtual head
+// h' = head * n_q + row sees keys t < len - (n_q - 1 - row) when causal.
+struct RowLimits {
+  int32_t head0, nh, len, n_q, causal;
+  __device__ __forceinline__ int32_t operator()(int32_t j) const {
+    if (j >= nh) return 0;
+    if (!causal || n_q <= 1) return len;
+    const int32_t lim = len - (n_q - 1 - (head0 + j) % n_q);
+    return lim < 0 ? 0 : lim;
+  }
 };
 
 template <int D_, class KV, int G_>
@@ -287,6 +301,7 @@ struct PieceIter {
     pc.tok_begin = (int32_t)(lo < L ? lo : L);
     pc.tok_end = (int32_t)(hi > pc.tok_begin ? hi : pc.tok_begin);
     pc.slot = s;
+    pc.len = L;
     return true;
   }
 };
@@ -470,6 +485,7 @@ struct CoreEngine {
   static constexpr int G = C::G, D = C::D, EPL = C::kEPL;
   float m[G], l[G];
   float2 o[G][EPL / 2];
+  int32_t lim[G];  // keys each head's row may see (the piece's row limits)
   uint32_t xr, pbase, e_nb;
   uint32_t voff[8];
   int warp, lane;
@@ -499,9 +515,13 @@ struct CoreEngine {
     }
   }
 
-  __device__ __forceinline__ void begin(uint32_t, float) {}
+  __device__ __forceinline__ void begin(uint32_t, float, const RowLimits& rl) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) lim[h] = rl(h);
+  }
 
-  __device__ __forceinline__ void tile(uint32_t kst, uint32_t vst, int nv, uint32_t qaddr, float qk_scale) {
+  __device__ __forceinline__ void tile(uint32_t kst, uint32_t vst, int nv, uint32_t qaddr, float qk_scale,
+                                       int32_t tok0) {
     // ---- q.k, lane = row
     float2 acc[G][C::kAcc];
 #pragma unroll
@@ -543,16 +563,17 @@ struct CoreEngine {
       }
     }
     // ---- online softmax over this warp's rows
-    const bool valid = lane < nv;
+    const int32_t key = tok0 + 32 * warp + lane;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       float s = 0.f;
 #pragma unroll
       for (int a = 0; a < C::kAcc; ++a) s += acc[h][a].x + acc[h][a].y;
-      s = valid ? s * qk_scale : -INFINITY;
+      s = (lane < nv && key < lim[h]) ? s * qk_scale : -INFINITY;
       const float mn = fmaxf(m[h], warp_max(s));
-      const float alpha = exp2f(m[h] - mn);
-      const float pr = exp2f(s - mn);
+      // a head whose row has seen no key yet keeps its empty state
+      const float alpha = mn == -INFINITY ? 1.f : exp2f(m[h] - mn);
+      const float pr = mn == -INFINITY ? 0.f : exp2f(s - mn);
       l[h] = fmaf(l[h], alpha, pr);
       const float2 al = make_float2(alpha, alpha);
 #pragma unroll
@@ -641,7 +662,8 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
         *abort_flag = 1;
       }
       const uint32_t qaddr = sbase + C::kQOff + qslot * C::kQBytes;
-      if (ok) eng.begin(qaddr, p.qk_scale);
+      const RowLimits rl{head0, nh, pc.len, p.n_q, p.causal};
+      if (ok) eng.begin(qaddr, p.qk_scale, rl);
       for (int32_t t0 = pc.tok_begin; ok && t0 < pc.tok_end; t0 += C::kBT, ++it) {
         const uint32_t stage = it % C::kStages;
         if (*abort_flag || !mbar_wait(full + stage, (it / C::kStages) & 1)) {
@@ -654,7 +676,7 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
         nv = nv < 0 ? 0 : (nv > 32 ? 32 : nv);
         if (nv > 0) {
           const uint32_t kst = sbase + stage * C::kStageBytes;
-          eng.tile(kst, kst + C::kTileBytes, nv, qaddr, p.qk_scale);
+          eng.tile(kst, kst + C::kTileBytes, nv, qaddr, p.qk_scale, t0);
         }
         if (lane == 0) mbar_arrive(empty + stage);
       }

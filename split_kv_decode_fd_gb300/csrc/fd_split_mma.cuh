@@ -81,6 +81,7 @@ struct MmaEngine {
   uint32_t qa[KS][4];  // A fragments of q (hi rows 0-7, lo rows 8-15) for each k-step
   float o[NT][4];      // p.V accumulators: [.][0..1] from p_hi, [.][2..3] from p_lo
   float m, mt, l;      // head g of this lane's quad: reference max, true max, partial sum of p
+  int32_t lim;         // keys head g's row may see
   int warp, lane, g, t;
   uint32_t kb[2], koff[KS];         // ldmatrix row address parts for K
   uint32_t vb[2], voffs[NT / 2];    // ... and for V (transposed)
@@ -123,7 +124,8 @@ struct MmaEngine {
   }
 
   // q rows of the piece (fp32 in shared memory), times scale*log2(e), split hi/lo.
-  __device__ __forceinline__ void begin(uint32_t qaddr, float qk_scale) {
+  __device__ __forceinline__ void begin(uint32_t qaddr, float qk_scale, const RowLimits& rl) {
+    lim = g < G ? rl(g) : 0;
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
       const uint32_t a = qaddr + (g * D + 16 * kk + 2 * t) * 4;
@@ -137,7 +139,7 @@ struct MmaEngine {
     }
   }
 
-  __device__ __forceinline__ void tile(uint32_t kst, uint32_t vst, int nv, uint32_t, float) {
+  __device__ __forceinline__ void tile(uint32_t kst, uint32_t vst, int nv, uint32_t, float, int32_t tok0) {
     if (nv < 32) {
       // Rows past the valid keys get p = 0, but 0 * NaN is NaN: clear those V rows.
       for (int r = nv; r < 32; ++r) {
@@ -179,7 +181,7 @@ struct MmaEngine {
       for (int j = 0; j < 2; ++j) {
         const int key = 8 * n + 2 * t + j;
         const float v = sc[n][j] + sc[n][j + 2];
-        s[n][j] = key < nv ? v : -INFINITY;
+        s[n][j] = (key < nv && tok0 + 32 * warp + key < lim) ? v : -INFINITY;
         smax = fmaxf(smax, s[n][j]);
       }
     smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
@@ -195,11 +197,13 @@ struct MmaEngine {
         for (int j = 0; j < 4; ++j) o[n][j] *= alpha;
       m = mn;
     }
+    // a head whose row has seen no key yet (m = -inf) gets p = 0 for every key
+    const float mref = m == -INFINITY ? 0.f : m;
     uint32_t pa[2][4];
 #pragma unroll
     for (int j2 = 0; j2 < 2; ++j2) {
-      const float p00 = exp2f(s[2 * j2][0] - m), p01 = exp2f(s[2 * j2][1] - m);
-      const float p10 = exp2f(s[2 * j2 + 1][0] - m), p11 = exp2f(s[2 * j2 + 1][1] - m);
+      const float p00 = exp2f(s[2 * j2][0] - mref), p01 = exp2f(s[2 * j2][1] - mref);
+      const float p10 = exp2f(s[2 * j2 + 1][0] - mref), p11 = exp2f(s[2 * j2 + 1][1] - mref);
       l += (p00 + p01) + (p10 + p11);
       split_bf16x2(p00, p01, pa[j2][0], pa[j2][1]);
       split_bf16x2(p10, p11, pa[j2][2], pa[j2][3]);

@@ -17,7 +17,7 @@ import numpy as np
 
 __all__ = [
     "FdError", "KvDesc", "library_path", "load_library", "workspace_bytes", "split_size", "plan_pieces",
-    "Workspace", "decode", "decode_host", "decode_static", "split_partial", "combine", "workspace_status",
+    "Workspace", "decode", "decode_rows", "decode_host", "decode_static", "split_partial", "combine", "workspace_status",
 ]
 
 FD_OK, FD_ERR_INVALID_ARG, FD_ERR_UNSUPPORTED, FD_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3
@@ -85,6 +85,8 @@ def load_library(path: Optional[str] = None):
             "fd_plan_pieces": (c_i64, [c_i32, c_i32, c_i32, vp, c_i32, c_i32, c_i32, vp, c_i64]),
             "fd_decode_static": (ctypes.c_int, [vp, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32, c_i32, f32,
                                                 c_i32, vp]),
+            "fd_decode_rows": (ctypes.c_int, [vp, c_i32, c_i32, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32,
+                                              c_i32, f32, c_i32, vp, c_sz, vp]),
             "fd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "fd_version": (c_i32, []),
         }
@@ -242,6 +244,41 @@ def decode(q, k, v, *, seq_lens=None, max_seq_len=None, block_table=None, scale=
                           B, Hq, Hkv, seq_lens.data_ptr() if seq_lens is not None else None, max_seq_len, D,
                           float(scale), int(n_splits), buf.data_ptr(), buf.numel(), _stream_handle(q.device, stream))
     _check(st, "fd_decode")
+    return out, lse
+
+
+def decode_rows(q, k, v, *, causal=True, seq_lens=None, max_seq_len=None, block_table=None, scale=None,
+                n_splits=FD_SPLITS_AUTO, out=None, lse=None, return_lse=True, workspace: Optional[Workspace] = None,
+                stream=None):
+    """``fd_decode_rows``: q ``[B, Hq, n_q, D]`` (n_q query rows per head); returns
+    ``(out [B, Hq, n_q, D], lse [B, Hq, n_q] or None)``.  With ``causal`` row i sees
+    keys ``t < L_b - (n_q - 1 - i)``.
+    """
+    torch = _torch()
+    _need_cuda(q, "q", torch.float32)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, Hq, n_q, D]")
+    kv = _kv_desc(k, v, block_table)
+    B, Hq, n_q, D = q.shape
+    Hkv = k.shape[1]
+    if max_seq_len is None:
+        max_seq_len = k.shape[2] if block_table is None else block_table.shape[1] * k.shape[2]
+    if seq_lens is not None:
+        _need_cuda(seq_lens, "seq_lens", torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, n_q, D), dtype=torch.float32, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, n_q), dtype=torch.float32, device=q.device)
+    ws = workspace or _default_workspace(q.device)
+    buf = ws.get(workspace_bytes(B, Hq * n_q, Hkv, D, n_splits), q.device)
+    st = _lib().fd_decode_rows(q.data_ptr(), int(n_q), int(bool(causal)), ctypes.byref(kv), out.data_ptr(),
+                               lse.data_ptr() if lse is not None else None, B, Hq, Hkv,
+                               seq_lens.data_ptr() if seq_lens is not None else None, int(max_seq_len), D,
+                               float(scale), int(n_splits), buf.data_ptr(), buf.numel(),
+                               _stream_handle(q.device, stream))
+    _check(st, "fd_decode_rows")
     return out, lse
 
 

@@ -213,3 +213,16 @@ def test_explicit_plan(lib):
         for cta, b, vkv, lo, hi, s, npieces in pieces:
             assert npieces == n
             assert lo == min(s * S, lens[b]) and hi == max(lo, min((s + 1) * S, lens[b]))
+
+
+@pytest.mark.parametrize("n_q,causal,expected", [
+    (0, 1, fdb.FD_ERR_INVALID_ARG),
+    (65, 1, fdb.FD_ERR_INVALID_ARG),
+    (2, 2, fdb.FD_ERR_INVALID_ARG),
+    (2, 1, fdb.FD_ERR_WORKSPACE_TOO_SMALL),  # valid window; the 1 KB workspace is what fails
+])
+def test_decode_rows_rejects_bad_window(lib, n_q, causal, expected):
+    kv = _kv()
+    st = lib.fd_decode_rows(FAKE, n_q, causal, ctypes.byref(kv), FAKE, None, 1, 4, 4, None, 1024, 128, 0.1, 4,
+                            FAKE, 1024, None)
+    assert st == expected
