@@ -158,8 +158,9 @@ FD_API fd_status fd_decode(const float* q, const fd_kv_desc* kv, float* out, flo
 
 /*
  * Decode with n_q query rows per (batch, head) sharing one read of K/V, for a
- * small batch of new tokens per sequence (e.g. verifying speculative tokens;
- * "FlashDecoding and split-KV" names one query row or a small batch of them).
+ * few new tokens per sequence (e.g. verifying speculative tokens): the page
+ * "FlashDecoding and split-KV", section "Walking through it", lets decode carry
+ * n_q slightly above one and leaves the masking of those rows open.
  *   q    [B, Hq, n_q, D] fp32; out [B, Hq, n_q, D]; lse [B, Hq, n_q] or NULL.
  *   causal = 1: the n_q rows are the last n_q tokens, already in the cache, and
  *            row i attends keys t < L_b - (n_q - 1 - i); causal = 0: every row
