@@ -423,7 +423,7 @@ def run_fdecode(args):
     gpd = fd.workspace_status(ws)
     g = spec.Hq * n_q // spec.Hkv
     gpad = 1
-    while gpad < g and gpad < 8:
+    while gpad < g and gpad < (16 if spec.kv_dtype == "bf16" else 8):
         gpad *= 2
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,

@@ -167,7 +167,8 @@ FD_API fd_status fd_decode(const float* q, const fd_kv_desc* kv, float* out, flo
  *            attends all L_b keys.  A row with no key gives out = 0, lse = -inf.
  *   1 <= n_q <= 64.  Other arguments as in fd_decode; the workspace is
  *   fd_workspace_bytes(B, Hq * n_q, Hkv, D, n_splits, 0).  The rows of a GQA
- *   group are served together (up to 8 rows x heads per K/V read).
+ *   group are served together (up to 16 rows x heads per bf16 K/V read, 8 per
+ *   fp32 read).
  */
 FD_API fd_status fd_decode_rows(const float* q, int32_t n_q, int32_t causal, const fd_kv_desc* kv, float* out,
                                 float* lse, int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_lens,
@@ -242,17 +243,19 @@ FD_API fd_status fd_decode_static(const float* q, const fd_kv_desc* kv, float* o
 /*
  * Host-side description of the work decomposition, for inspection and tests
  * (touches no GPU).  Enumerates every split piece that fd_decode would run
- * for these lengths on `grid` CTAs (FD_SPLITS_AUTO) or for n_splits > 0.
+ * for these lengths on `grid` CTAs (FD_SPLITS_AUTO) or for n_splits > 0, for
+ * a cache of dtype kv_dtype (an fd_dtype).
  * Each piece is 7 int32: {cta, b, virtual_kv_head, tok_begin, tok_end, slot,
  * pieces_of_its_sequence} (the last is the arrival count that triggers the
- * fused merge).  A virtual KV head is a KV head with up to 8 of its query
- * heads; when Hq / Hkv <= 8 it is the KV head itself.
+ * fused merge).  A virtual KV head is a KV head with up to 16 (bf16 cache) or
+ * 8 (fp32 cache) of its query heads; when Hq / Hkv is at most that, it is the
+ * KV head itself.
  * Writes at most `capacity` pieces and returns the total count (negative on
  * bad arguments).  seq_lens_host may be NULL (every L_b = max_seq_len).
  */
-FD_API int64_t fd_plan_pieces(int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_lens_host,
-                       int32_t max_seq_len, int32_t n_splits, int32_t grid, int32_t* pieces,
-                       int64_t capacity);
+FD_API int64_t fd_plan_pieces(int32_t B, int32_t Hq, int32_t Hkv, int32_t kv_dtype, const int32_t* seq_lens_host,
+                              int32_t max_seq_len, int32_t n_splits, int32_t grid, int32_t* pieces,
+                              int64_t capacity);
 
 /* Static description of a status code. */
 FD_API const char* fd_status_string(fd_status status);

@@ -53,8 +53,10 @@ struct WsLayout {
 };
 
 // Workspace: [header | counters | o | m | l | host staging (q, out, lse, lens)].
-WsLayout ws_layout(int B, int Hq, int Hkv, int D, int n_splits, int grid) {
-  const Groups gr = make_groups(Hq, Hkv);
+int group_cap(int dtype) { return dtype == FD_BF16 ? kMaxGroupBf16 : kMaxGroupF32; }
+
+WsLayout ws_layout(int B, int Hq, int Hkv, int D, int n_splits, int grid, int cap) {
+  const Groups gr = make_groups(Hq, Hkv, cap);
   const size_t pairs = (size_t)B * gr.hv;
   size_t states;  // number of (slot, head) partial states
   if (n_splits == 0)
@@ -78,7 +80,7 @@ WsLayout ws_layout(int B, int Hq, int Hkv, int D, int n_splits, int grid) {
 fd_status check_shape(int B, int Hq, int Hkv, int D) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FD_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FD_ERR_UNSUPPORTED;
-  const Groups gr = make_groups(Hq, Hkv);
+  const Groups gr = make_groups(Hq, Hkv, kMaxGroupF32);  // the larger hv of the two caps
   if ((int64_t)B * gr.hv > (int64_t)1 << 30) return FD_ERR_UNSUPPORTED;
   return FD_OK;
 }
@@ -89,7 +91,7 @@ fd_status check_kv(const fd_kv_desc* kv, int B, int Hkv, int max_seq_len) {
   if (kv->dtype != FD_F32 && kv->dtype != FD_BF16) return FD_ERR_UNSUPPORTED;
   if (max_seq_len < 0) return FD_ERR_INVALID_ARG;
   const int64_t tiles = (int64_t)B * Hkv * ((max_seq_len + kPlanTile - 1) / kPlanTile);
-  if (tiles >= ((int64_t)1 << 31) / kMaxGroup) return FD_ERR_UNSUPPORTED;
+  if (tiles >= ((int64_t)1 << 31) / kMaxGroupBf16) return FD_ERR_UNSUPPORTED;
   if (kv->layout == FD_KV_CONTIGUOUS) {
     if (kv->capacity < 1 || kv->capacity < max_seq_len) return FD_ERR_INVALID_ARG;
     if (kv->capacity > ((int64_t)1 << 31) - 1) return FD_ERR_UNSUPPORTED;
@@ -168,7 +170,7 @@ SplitParams base_params(const float* q, const fd_kv_desc* kv, int B, int Hq, int
                         const int32_t* seq_lens, int max_seq_len, float scale) {
   SplitParams p;
   std::memset(&p, 0, sizeof(p));
-  const Groups gr = make_groups(Hq, Hkv);
+  const Groups gr = make_groups(Hq, Hkv, group_cap(kv->dtype));
   p.q = q;
   p.seq_lens = seq_lens;
   p.B = B;
@@ -245,13 +247,19 @@ size_t fd_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t
   if (check_shape(B, Hq, Hkv, D) != FD_OK || n_splits < 0 || n_splits > 65535) return 0;
   int grid = num_sms;
   if (grid <= 0 && !sm_count(&grid)) return 0;
-  const Groups gr = make_groups(Hq, Hkv);
-  if (n_splits == 0 && (B > FD_AUTO_MAX_BATCH || (int64_t)B * gr.hv > kMaxFusedPairs)) {
-    // the fallback split count depends on max_seq_len; size for the largest it can be
-    const size_t a = ws_layout(B, Hq, Hkv, D, fallback_splits(B, gr.hv, 1 << 30, grid), grid).total;
-    return a;
+  // The size must hold for either cache dtype (their group caps differ).
+  size_t most = 0;
+  for (const int cap : {kMaxGroupF32, kMaxGroupBf16}) {
+    const Groups gr = make_groups(Hq, Hkv, cap);
+    size_t a;
+    if (n_splits == 0 && (B > FD_AUTO_MAX_BATCH || (int64_t)B * gr.hv > kMaxFusedPairs))
+      // the fallback split count depends on max_seq_len; size for the largest it can be
+      a = ws_layout(B, Hq, Hkv, D, fallback_splits(B, gr.hv, 1 << 30, grid), grid, cap).total;
+    else
+      a = ws_layout(B, Hq, Hkv, D, n_splits, grid, cap).total;
+    most = a > most ? a : most;
   }
-  return ws_layout(B, Hq, Hkv, D, n_splits, grid).total;
+  return most;
 }
 
 fd_status fd_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
@@ -289,14 +297,14 @@ fd_status decode_impl(const float* q, const fd_kv_desc* kv, float* out, float* l
     return FD_ERR_INVALID_ARG;
   if (n_splits < 0 || n_splits > 65535) return FD_ERR_INVALID_ARG;
   if ((st = check_kv(kv, B, Hkv, max_seq_len)) != FD_OK) return st;
-  const Groups gr = make_groups(Hq, Hkv);
+  const Groups gr = make_groups(Hq, Hkv, group_cap(kv->dtype));
   const int64_t pairs = (int64_t)B * gr.hv;
   int sms = 0;
   if (n_splits == 0) {
     if (!sm_count(&sms)) return FD_ERR_CUDA;
     if (B > FD_AUTO_MAX_BATCH || pairs > kMaxFusedPairs) n_splits = fallback_splits(B, gr.hv, max_seq_len, sms);
   }
-  const WsLayout w = ws_layout(B, Hq, Hkv, D, n_splits, sms);
+  const WsLayout w = ws_layout(B, Hq, Hkv, D, n_splits, sms, group_cap(kv->dtype));
   if (workspace_bytes < w.total) return FD_ERR_WORKSPACE_TOO_SMALL;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -388,11 +396,13 @@ fd_status fd_decode_host(const float* q_host, const fd_kv_desc* kv, float* out_h
   if (n_splits < 0 || n_splits > 65535) return FD_ERR_INVALID_ARG;
   int grid_ctas = 0;
   if (n_splits == 0 && !sm_count(&grid_ctas)) return FD_ERR_CUDA;
+  if (!kv) return FD_ERR_INVALID_ARG;
+  if (kv->dtype != FD_F32 && kv->dtype != FD_BF16) return FD_ERR_UNSUPPORTED;
   int n_eff = n_splits;
-  const Groups gr = make_groups(Hq, Hkv);
+  const Groups gr = make_groups(Hq, Hkv, group_cap(kv->dtype));
   if (n_splits == 0 && (B > FD_AUTO_MAX_BATCH || (int64_t)B * gr.hv > kMaxFusedPairs))
     n_eff = fallback_splits(B, gr.hv, max_seq_len, grid_ctas);
-  const WsLayout w = ws_layout(B, Hq, Hkv, D, n_eff, grid_ctas);
+  const WsLayout w = ws_layout(B, Hq, Hkv, D, n_eff, grid_ctas, group_cap(kv->dtype));
   if (workspace_bytes < w.total) return FD_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = (cudaStream_t)stream;
@@ -415,10 +425,11 @@ fd_status fd_decode_host(const float* q_host, const fd_kv_desc* kv, float* out_h
   return cudaStreamSynchronize(s) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
-int64_t fd_plan_pieces(int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_lens_host, int32_t max_seq_len,
-                       int32_t n_splits, int32_t grid, int32_t* pieces, int64_t capacity) {
+int64_t fd_plan_pieces(int32_t B, int32_t Hq, int32_t Hkv, int32_t kv_dtype, const int32_t* seq_lens_host,
+                       int32_t max_seq_len, int32_t n_splits, int32_t grid, int32_t* pieces, int64_t capacity) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_seq_len < 0 || n_splits < 0) return -1;
-  const Groups gr = make_groups(Hq, Hkv);
+  if (kv_dtype != FD_F32 && kv_dtype != FD_BF16) return -1;
+  const Groups gr = make_groups(Hq, Hkv, group_cap(kv_dtype));
   std::vector<int32_t> ln(B), pre(B + 1, 0);
   for (int b = 0; b < B; ++b) ln[b] = clamp_len(seq_lens_host ? seq_lens_host[b] : max_seq_len, max_seq_len);
   for (int b = 0; b < B; ++b) pre[b + 1] = pre[b] + ceil_div(ln[b], kPlanTile);
@@ -516,14 +527,14 @@ extern "C" fd_status fd_decode_static(const float* q, const fd_kv_desc* kv, floa
   if (!q || !out || !aligned16(q) || !aligned16(out)) return FD_ERR_INVALID_ARG;
   if (n_splits < 0 || n_splits > 65535) return FD_ERR_INVALID_ARG;
   if ((st = check_kv(kv, B, Hkv, max_seq_len)) != FD_OK) return st;
-  const Groups gr = make_groups(Hq, Hkv);
+  const Groups gr = make_groups(Hq, Hkv, group_cap(kv->dtype));
   const int64_t pairs = (int64_t)B * gr.hv;
   int sms = 0;
   if (n_splits == 0) {
     if (!sm_count(&sms)) return FD_ERR_CUDA;
     if (B > FD_AUTO_MAX_BATCH || pairs > kMaxFusedPairs) n_splits = fallback_splits(B, gr.hv, max_seq_len, sms);
   }
-  const WsLayout w = ws_layout(B, Hq, Hkv, D, n_splits, sms);
+  const WsLayout w = ws_layout(B, Hq, Hkv, D, n_splits, sms, group_cap(kv->dtype));
   // Only the scratch part of the layout is used here (no host staging area).
   if (w.q_stage > kStaticScratchBytes) return FD_ERR_WORKSPACE_TOO_SMALL;
   void* base = nullptr;

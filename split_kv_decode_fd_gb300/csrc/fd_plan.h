@@ -17,8 +17,9 @@
 //    whatever the mix of lengths.
 //
 // A "virtual kv head" is one KV head together with a sub-group of at most
-// kMaxGroup of the query heads that share it; when g <= kMaxGroup there is
-// one sub-group per KV head.
+// max_group of the query heads that share it (16 for bf16 caches, whose
+// tensor-core engine takes sixteen heads; 8 for fp32); when g <= max_group
+// there is one sub-group per KV head.
 //
 // The balanced plan uses G = min(CTAs launched, T) CTAs, so that every range
 // holds at least one tile and the CTAs holding one sequence are consecutive;
@@ -42,7 +43,8 @@
 namespace fdk {
 
 constexpr int kPlanTile = 128;   // tokens per balancing tile
-constexpr int kMaxGroup = 8;     // query heads served by one CTA from one K/V read
+constexpr int kMaxGroupF32 = 8;   // query heads served by one CTA from one fp32 K/V read
+constexpr int kMaxGroupBf16 = 16; // ... from one bf16 K/V read
 constexpr int kSplitAlign = 16;  // explicit split sizes are multiples of this
 
 FD_HD int32_t ceil_div(int32_t a, int32_t b) { return (a + b - 1) / b; }
@@ -67,11 +69,11 @@ struct Groups {
   int32_t hv;      // virtual KV heads per sequence = Hkv * nsub
 };
 
-FD_HD Groups make_groups(int32_t Hq, int32_t Hkv) {
+FD_HD Groups make_groups(int32_t Hq, int32_t Hkv, int32_t max_group) {
   Groups r;
   r.g = Hq / Hkv;
   int32_t gp = 1;
-  while (gp < r.g && gp < kMaxGroup) gp *= 2;
+  while (gp < r.g && gp < max_group) gp *= 2;
   r.gpad = gp;
   r.nsub = ceil_div(r.g, gp);
   r.hv = Hkv * r.nsub;

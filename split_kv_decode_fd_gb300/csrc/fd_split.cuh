@@ -103,22 +103,30 @@ struct SplitCfg {
   static constexpr int kAcc = G >= 8 ? 1 : 8 / G;
   static constexpr int kBoxBytes = 16 * 128;
 
-  // bf16 caches with four or eight query heads per CTA run q.k and p.V on
+  // bf16 caches with four or more query heads per CTA run q.k and p.V on
   // mma.sync; there the CUDA-core FMAs (and bf16 widening) bound the kernel
   // well above its streaming time, while one or two heads per CTA stay cheap.
   static constexpr bool kMma = kBf16 && G >= 4;
+  // Sixteen heads per CTA (bf16 only): each lane's MMA fragments carry two
+  // heads.  q lives in registers after the first read, so one q buffer is
+  // enough (released as soon as every warp has its fragments), and the warp
+  // states are merged eight heads at a time to keep the merge buffer small.
+  static constexpr bool kWide = G > 8;
+  static constexpr int kQBufs = kWide ? 1 : 2;
+  static constexpr int kPubHeads = kWide ? 8 : G;  // heads per merge round
+  static_assert(!kWide || (kBf16 && G == 16), "sixteen heads per CTA need a bf16 cache");
   static_assert(kNB >= 1 && kStages >= 2, "unsupported row size");
 
   // shared-memory layout (byte offsets from a 1024-aligned base)
   static constexpr int kQOff = kStages * kStageBytes;
   static constexpr int kQBytes = G * D * 4;
-  static constexpr int kUOff = kQOff + 2 * kQBytes;
-  static constexpr int kPBytes = kWarps * 32 * G * 8;
-  static constexpr int kObBytes = kWarps * G * D * 4;
+  static constexpr int kUOff = kQOff + kQBufs * kQBytes;
+  static constexpr int kPBytes = kMma ? 0 : kWarps * 32 * G * 8;  // CUDA-core engine's p rows
+  static constexpr int kObBytes = kWarps * kPubHeads * D * 4;
   static constexpr int kUBytes = kPBytes > kObBytes ? kPBytes : kObBytes;
   static constexpr int kMlOff = kUOff + kUBytes;
-  static constexpr int kFinOff = kMlOff + kWarps * G * 8;
-  static constexpr int kLenOff = kFinOff + G * 8;
+  static constexpr int kFinOff = kMlOff + kWarps * kPubHeads * 8;
+  static constexpr int kLenOff = kFinOff + kPubHeads * 8;
   static constexpr int kPreOff = kLenOff + (kAutoMaxBatch + 4) * 4;
   static constexpr int kBarOff = kPreOff + (kAutoMaxBatch + 4) * 4;
   static constexpr int kFlagOff = kBarOff + (2 * kStages + 4) * 8;
@@ -333,8 +341,8 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
     vkv_heads(gr, pc.vkv, &head0, &nh);
     const int32_t kvh = kv_head_of_vkv(gr, pc.vkv);
     if (lane == 0) {
-      const uint32_t slot = qi & 1;
-      if (!mbar_wait(qempty + slot, ((qi >> 1) & 1) ^ 1)) ok = false;
+      const uint32_t slot = qi % C::kQBufs;
+      if (!mbar_wait(qempty + slot, ((qi / C::kQBufs) & 1) ^ 1)) ok = false;
       if (ok) {
         const uint32_t bytes = (uint32_t)nh * C::D * 4;
         mbar_arrive_expect_tx(qfull + slot, bytes);
@@ -593,7 +601,7 @@ struct CoreEngine {
   }
 
   // Warp state -> merge slot `warp`: O[h][:] (unnormalised, on m[h]), m[h], l[h].
-  __device__ __forceinline__ void publish(float* obuf, float* mlbuf) {
+  __device__ __forceinline__ void publish(float* obuf, float* mlbuf, int) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const float lw = warp_sum(l[h]);
@@ -655,15 +663,20 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
     vkv_heads(gr, pc.vkv, &head0, &nh);
     const bool nonempty = pc.tok_end > pc.tok_begin;
     eng.reset();
-    const uint32_t qslot = qi & 1;
+    const uint32_t qslot = qi % C::kQBufs;
     if (nonempty && ok) {
-      if (!mbar_wait(qfull + qslot, (qi >> 1) & 1)) {
+      if (!mbar_wait(qfull + qslot, (qi / C::kQBufs) & 1)) {
         ok = false;
         *abort_flag = 1;
       }
       const uint32_t qaddr = sbase + C::kQOff + qslot * C::kQBytes;
       const RowLimits rl{head0, nh, pc.len, p.n_q, p.causal};
       if (ok) eng.begin(qaddr, p.qk_scale, rl);
+      if constexpr (C::kWide) {
+        // q is in registers now: hand the buffer back (one arrival per warp)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qempty + qslot);
+      }
       for (int32_t t0 = pc.tok_begin; ok && t0 < pc.tok_end; t0 += C::kBT, ++it) {
         const uint32_t stage = it % C::kStages;
         if (*abort_flag || !mbar_wait(full + stage, (it / C::kStages) & 1)) {
@@ -684,26 +697,10 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
 
     // ---- merge the W warp states of this piece
     named_barrier(1, kCons);  // every warp is past its last tile: the p buffers may be reused
-    if (nonempty && tid == 0) mbar_arrive(qempty + qslot);
-    if (nonempty) ++qi;
-    eng.publish(obuf, mlbuf);
-    named_barrier(1, kCons);
-    if (tid < G) {
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < W; ++w) M = fmaxf(M, mlbuf[(w * G + tid) * 2]);
-      float L = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < W; ++w) {
-          const float mw = mlbuf[(w * G + tid) * 2];
-          if (mw != -INFINITY) L = fmaf(exp2f(mw - M), mlbuf[(w * G + tid) * 2 + 1], L);
-        }
-      }
-      fin[tid * 2] = M;
-      fin[tid * 2 + 1] = L;
+    if constexpr (!C::kWide) {
+      if (nonempty && tid == 0) mbar_arrive(qempty + qslot);
     }
-    named_barrier(1, kCons);
+    if (nonempty) ++qi;
 
     // Does this piece hold the whole sequence?  Then it is the output.
     int npieces = 1;
@@ -718,37 +715,64 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
     }
     const bool final_here = fused && npieces == 1;
 
-    for (int idx = tid; idx < G * D; idx += kCons) {
-      const int h = idx / D, d = idx % D;
-      if (h >= nh) continue;
-      const float M = fin[h * 2];
-      float acc = 0.f;
-      if (M != -INFINITY) {
+    // kPubHeads heads per round; rounds > 1 only with sixteen heads per CTA
+    constexpr int PH = C::kPubHeads;
+#pragma unroll 1
+    for (int r = 0; r < G / PH; ++r) {
+      if (r > 0) named_barrier(1, kCons);  // the last round's readers are done with the buffers
+      eng.publish(obuf, mlbuf, r);
+      named_barrier(1, kCons);
+      if (tid < PH) {
+        float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < W; ++w) {
-          const float mw = mlbuf[(w * G + h) * 2];
-          if (mw != -INFINITY) acc = fmaf(exp2f(mw - M), obuf[(w * G + h) * D + d], acc);
+        for (int w = 0; w < W; ++w) M = fmaxf(M, mlbuf[(w * PH + tid) * 2]);
+        float L = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < W; ++w) {
+            const float mw = mlbuf[(w * PH + tid) * 2];
+            if (mw != -INFINITY) L = fmaf(exp2f(mw - M), mlbuf[(w * PH + tid) * 2 + 1], L);
+          }
+        }
+        fin[tid * 2] = M;
+        fin[tid * 2 + 1] = L;
+      }
+      named_barrier(1, kCons);
+
+      for (int idx = tid; idx < PH * D; idx += kCons) {
+        const int hl = idx / D, d = idx % D;
+        const int h = r * PH + hl;
+        if (h >= nh) continue;
+        const float M = fin[hl * 2];
+        float acc = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < W; ++w) {
+            const float mw = mlbuf[(w * PH + hl) * 2];
+            if (mw != -INFINITY) acc = fmaf(exp2f(mw - M), obuf[(w * PH + hl) * D + d], acc);
+          }
+        }
+        if (final_here) {
+          const float L = fin[hl * 2 + 1];
+          p.out[((size_t)pc.b * p.Hq + head0 + h) * D + d] = M == -INFINITY ? 0.f : acc / L;
+        } else if (balanced) {
+          p.o_part[((size_t)pc.slot * G + h) * D + d] = acc;
+        } else {
+          p.o_part[(((size_t)pc.b * p.Hq + head0 + h) * p.n_splits + pc.slot) * D + d] = acc;
         }
       }
-      if (final_here) {
-        const float L = fin[h * 2 + 1];
-        p.out[((size_t)pc.b * p.Hq + head0 + h) * D + d] = M == -INFINITY ? 0.f : acc / L;
-      } else if (balanced) {
-        p.o_part[((size_t)pc.slot * G + h) * D + d] = acc;
-      } else {
-        p.o_part[(((size_t)pc.b * p.Hq + head0 + h) * p.n_splits + pc.slot) * D + d] = acc;
-      }
-    }
-    if (tid < nh) {
-      const float M = fin[tid * 2], L = fin[tid * 2 + 1];
-      const float m_nat = M == -INFINITY ? -INFINITY : M * kLn2;
-      if (final_here) {
-        if (p.lse) p.lse[(size_t)pc.b * p.Hq + head0 + tid] = M == -INFINITY ? -INFINITY : m_nat + logf(L);
-      } else {
-        const size_t i = balanced ? (size_t)pc.slot * G + tid
-                                  : ((size_t)pc.b * p.Hq + head0 + tid) * p.n_splits + pc.slot;
-        p.m_part[i] = m_nat;
-        p.l_part[i] = L;
+      if (tid < PH && r * PH + tid < nh) {
+        const int h = r * PH + tid;
+        const float M = fin[tid * 2], L = fin[tid * 2 + 1];
+        const float m_nat = M == -INFINITY ? -INFINITY : M * kLn2;
+        if (final_here) {
+          if (p.lse) p.lse[(size_t)pc.b * p.Hq + head0 + h] = M == -INFINITY ? -INFINITY : m_nat + logf(L);
+        } else {
+          const size_t i = balanced ? (size_t)pc.slot * G + h
+                                    : ((size_t)pc.b * p.Hq + head0 + h) * p.n_splits + pc.slot;
+          p.m_part[i] = m_nat;
+          p.l_part[i] = L;
+        }
       }
     }
 
@@ -816,8 +840,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(bars + C::kStages + s, C::kWarps);    // empty: one arrival per consumer warp
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bars + 2 * C::kStages + i, 1);        // q full
-      mbar_init(bars + 2 * C::kStages + 2 + i, 1);    // q empty
+      mbar_init(bars + 2 * C::kStages + i, 1);                               // q full
+      mbar_init(bars + 2 * C::kStages + 2 + i, C::kWide ? C::kWarps : 1);    // q empty
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -827,7 +851,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     prefetch_tensormap(&tmap_v);
   }
   // q rows past the live heads of a group must hold finite values.
-  for (int i = tid; i < 2 * C::G * C::D; i += C::kThreads)
+  for (int i = tid; i < C::kQBufs * C::G * C::D; i += C::kThreads)
     reinterpret_cast<float*>(smem + C::kQOff)[i] = 0.f;
 
   CtaTiles tl;
@@ -867,6 +891,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
   if (warp == C::kWarps)
     producer_warp<C>(&tmap_k, &tmap_v, p, tl, total, smem, abort_flag);
+  else if constexpr (C::kWide)
+    consumer_warps<C, MmaEngine16<C>>(p, tl, total, smem, abort_flag);
   else if constexpr (C::kMma)
     consumer_warps<C, MmaEngine<C>>(p, tl, total, smem, abort_flag);
   else

@@ -32,6 +32,9 @@ cudaError_t launch_split_dispatch(int D, int gpad, const CUtensorMap& tk, const 
   if (D == DD && gpad == GG) return launch_split_t<DD, KV, GG>(tk, tv, p, grid, stream);
   FD_CASE(128, 1) FD_CASE(128, 2) FD_CASE(128, 4) FD_CASE(128, 8)
   FD_CASE(64, 1) FD_CASE(64, 2) FD_CASE(64, 4) FD_CASE(64, 8)
+  if constexpr (sizeof(KV) == 2) {
+    FD_CASE(128, 16) FD_CASE(64, 16)
+  }
 #undef FD_CASE
   return cudaErrorInvalidValue;
 }

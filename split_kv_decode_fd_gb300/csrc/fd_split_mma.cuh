@@ -223,7 +223,7 @@ struct MmaEngine {
   }
 
   // Warp state -> merge slot `warp`, moved onto the true max of each head.
-  __device__ __forceinline__ void publish(float* obuf, float* mlbuf) {
+  __device__ __forceinline__ void publish(float* obuf, float* mlbuf, int) {
     const float f = m == -INFINITY ? 0.f : exp2f(m - mt);
     float ls = l + __shfl_xor_sync(0xffffffffu, l, 1);
     ls += __shfl_xor_sync(0xffffffffu, ls, 2);
@@ -235,6 +235,210 @@ struct MmaEngine {
     if (t == 0) {
       mlbuf[(warp * G + g) * 2] = mt;
       mlbuf[(warp * G + g) * 2 + 1] = ls * f;
+    }
+  }
+};
+
+// Sixteen heads per CTA (GQA groups of 16, or several query rows per head):
+// all sixteen rows of the M axis are heads, so q and p each take two MMAs,
+// one for the bf16 hi part and one for the lo part, accumulated into the same
+// fp32 registers.  Lane (g, t) holds heads g (C/A rows 0-7) and g + 8 (rows
+// 8-15); everything else -- stage layout, ldmatrix addressing, V-row clearing,
+// lazy rescaling -- follows MmaEngine.  Per head and key the MMA work is the
+// same as there; the K/V tile is read once for all sixteen heads.
+template <class C>
+struct MmaEngine16 {
+  static constexpr int D = C::D;
+  static constexpr int KS = D / 16;
+  static constexpr int NT = D / 8;
+  static constexpr int kRowStride = 128;
+  static constexpr int kBlk = C::kBT * 128;
+  static_assert(C::G == 16 && C::kBf16 && C::kBT == 128 && C::kWarps == 4, "MMA-16 engine layout");
+
+  uint32_t qh[KS][4], ql[KS][4];  // A fragments of q: hi and lo parts, rows = heads 0-15
+  float o[NT][4];                 // p.V accumulators: [.][0..1] head g, [.][2..3] head g + 8
+  float m[2], mt[2], l[2];        // heads g, g + 8: reference max, true max, partial sum
+  int32_t lim[2];                 // keys each of the two heads' rows may see
+  int warp, lane, g, t;
+  uint32_t kb[2], vb[2];  // ldmatrix row addresses (K, V transposed)
+  uint32_t kx, vx;        // this lane's swizzle term of the 16-byte chunk index, times 16
+  uint32_t zoff;
+
+  // Byte offset of 16-byte chunk pair `c` (k-step or d-pair index) within a
+  // swizzled row: chunk 2c + (lane bit) of block c / 4, XOR-swizzled by row.
+  static __device__ __forceinline__ uint32_t chunk_off(int c, uint32_t x) {
+    return (uint32_t)(c >> 2) * kBlk + (((uint32_t)(2 * (c & 3)) << 4) ^ x);
+  }
+
+  __device__ __forceinline__ void setup(int warp_, int lane_, uint8_t*) {
+    warp = warp_;
+    lane = lane_;
+    g = lane >> 2;
+    t = lane & 3;
+    const int mi = lane >> 3, r = lane & 7;
+    // K: matrix mi covers keys [8*(mi>>1), +8) and chunk (mi&1) of the k-step;
+    // V (transposed): keys [8*(mi&1), +8) and d-chunk (mi>>1) of the pair
+#pragma unroll
+    for (int np = 0; np < 2; ++np) kb[np] = (32 * warp + 16 * np + (mi >> 1) * 8 + r) * kRowStride;
+#pragma unroll
+    for (int j2 = 0; j2 < 2; ++j2) vb[j2] = (32 * warp + 16 * j2 + (mi & 1) * 8 + r) * kRowStride;
+    kx = (uint32_t)((mi & 1) ^ r) << 4;
+    vx = (uint32_t)((mi >> 1) ^ r) << 4;
+    const int zb = lane * (D / 16);
+    zoff = (zb / 128) * kBlk + (zb % 128);
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      m[i] = -INFINITY;
+      mt[i] = -INFINITY;
+      l[i] = 0.f;
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[n][j] = 0.f;
+  }
+
+  __device__ __forceinline__ void begin(uint32_t qaddr, float qk_scale, const RowLimits& rl) {
+    lim[0] = rl(g);
+    lim[1] = rl(g + 8);
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      const uint32_t a = qaddr + (g * D + 16 * kk + 2 * t) * 4;
+      const uint32_t b = a + 8 * D * 4;  // row g + 8
+      const float2 x0 = lds64f(a), x1 = lds64f(a + 32);
+      const float2 y0 = lds64f(b), y1 = lds64f(b + 32);
+      split_bf16x2(x0.x * qk_scale, x0.y * qk_scale, qh[kk][0], ql[kk][0]);  // row g,     k 2t..
+      split_bf16x2(y0.x * qk_scale, y0.y * qk_scale, qh[kk][1], ql[kk][1]);  // row g + 8, k 2t..
+      split_bf16x2(x1.x * qk_scale, x1.y * qk_scale, qh[kk][2], ql[kk][2]);  // row g,     k 2t+8..
+      split_bf16x2(y1.x * qk_scale, y1.y * qk_scale, qh[kk][3], ql[kk][3]);  // row g + 8, k 2t+8..
+    }
+  }
+
+  __device__ __forceinline__ void tile(uint32_t kst, uint32_t vst, int nv, uint32_t, float, int32_t tok0) {
+    if (nv < 32) {
+      // Rows past the valid keys get p = 0, but 0 * NaN is NaN: clear those V rows.
+      for (int r = nv; r < 32; ++r) {
+        const uint32_t a = vst + (32 * warp + r) * kRowStride + zoff;
+        if constexpr (D == 128)
+          asm volatile("st.shared.v2.u32 [%0], {%1, %1};" ::"r"(a), "r"(0u) : "memory");
+        else
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(0u) : "memory");
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+    }
+    const bool two = nv > 16;
+    // ---- q.k: hi and lo parts accumulate into the same registers
+    float sc[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sc[n][j] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kst + kb[0] + chunk_off(kk, kx), b0, b1, b2, b3);
+      mma_bf16_16816(sc[0], qh[kk], b0, b1);
+      mma_bf16_16816(sc[1], qh[kk], b2, b3);
+      mma_bf16_16816(sc[0], ql[kk], b0, b1);
+      mma_bf16_16816(sc[1], ql[kk], b2, b3);
+      if (two) {
+        ldsm_x4(kst + kb[1] + chunk_off(kk, kx), b0, b1, b2, b3);
+        mma_bf16_16816(sc[2], qh[kk], b0, b1);
+        mma_bf16_16816(sc[3], qh[kk], b2, b3);
+        mma_bf16_16816(sc[2], ql[kk], b0, b1);
+        mma_bf16_16816(sc[3], ql[kk], b2, b3);
+      }
+    }
+    // ---- online softmax, heads g (i = 0) and g + 8 (i = 1)
+    float s[2][4][2];
+    float smax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int key = 8 * n + 2 * t + j;
+        const bool in = key < nv;
+        const int32_t tok = tok0 + 32 * warp + key;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          s[i][n][j] = (in && tok < lim[i]) ? sc[n][2 * i + j] : -INFINITY;
+          smax[i] = fmaxf(smax[i], s[i][n][j]);
+        }
+      }
+    float mref[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      smax[i] = fmaxf(smax[i], __shfl_xor_sync(0xffffffffu, smax[i], 1));
+      smax[i] = fmaxf(smax[i], __shfl_xor_sync(0xffffffffu, smax[i], 2));
+      mt[i] = fmaxf(mt[i], smax[i]);
+      if (smax[i] > m[i] + kMmaTau) {
+        const float mn = fmaxf(m[i], smax[i]);
+        const float alpha = exp2f(m[i] - mn);
+        l[i] *= alpha;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          o[n][2 * i] *= alpha;
+          o[n][2 * i + 1] *= alpha;
+        }
+        m[i] = mn;
+      }
+      // a head whose row has seen no key yet (m = -inf) gets p = 0 for every key
+      mref[i] = m[i] == -INFINITY ? 0.f : m[i];
+    }
+    // p as A fragments: a0 = (row g, keys 2t..), a1 = (row g+8, keys 2t..),
+    // a2 = (row g, keys 2t+8..), a3 = (row g+8, keys 2t+8..) of each 16-key chunk
+    uint32_t ph[2][4], pl[2][4];
+#pragma unroll
+    for (int j2 = 0; j2 < 2; ++j2) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float p0 = exp2f(s[i][2 * j2][0] - mref[i]), p1 = exp2f(s[i][2 * j2][1] - mref[i]);
+        const float p2 = exp2f(s[i][2 * j2 + 1][0] - mref[i]), p3 = exp2f(s[i][2 * j2 + 1][1] - mref[i]);
+        l[i] += (p0 + p1) + (p2 + p3);
+        split_bf16x2(p0, p1, ph[j2][i], pl[j2][i]);
+        split_bf16x2(p2, p3, ph[j2][2 + i], pl[j2][2 + i]);
+      }
+    }
+    // ---- p.V
+#pragma unroll
+    for (int j2 = 0; j2 < 2; ++j2) {
+      if (j2 == 1 && !two) break;
+#pragma unroll
+      for (int np = 0; np < NT / 2; ++np) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vst + vb[j2] + chunk_off(np, vx), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * np], ph[j2], b0, b1);
+        mma_bf16_16816(o[2 * np + 1], ph[j2], b2, b3);
+        mma_bf16_16816(o[2 * np], pl[j2], b0, b1);
+        mma_bf16_16816(o[2 * np + 1], pl[j2], b2, b3);
+      }
+    }
+  }
+
+  // Round r publishes heads 8r..8r+7 (this lane's head g + 8r) into merge
+  // slot `warp`, moved onto the true max.
+  __device__ __forceinline__ void publish(float* obuf, float* mlbuf, int r) {
+    const bool hi = r != 0;
+    const float mi = hi ? m[1] : m[0];
+    const float mti = hi ? mt[1] : mt[0];
+    const float li = hi ? l[1] : l[0];
+    const float f = mi == -INFINITY ? 0.f : exp2f(mi - mti);
+    float ls = li + __shfl_xor_sync(0xffffffffu, li, 1);
+    ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+    float* row = obuf + (warp * 8 + g) * D + 2 * t;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const float a = hi ? o[n][2] : o[n][0];
+      const float b = hi ? o[n][3] : o[n][1];
+      *reinterpret_cast<float2*>(row + 8 * n) = make_float2(a * f, b * f);
+    }
+    if (t == 0) {
+      mlbuf[(warp * 8 + g) * 2] = mti;
+      mlbuf[(warp * 8 + g) * 2 + 1] = ls * f;
     }
   }
 };

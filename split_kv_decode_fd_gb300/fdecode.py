@@ -82,7 +82,7 @@ def load_library(path: Optional[str] = None):
             "fd_combine": (ctypes.c_int, [vp, vp, vp, vp, vp, c_i32, c_i32, c_i32, c_i32, vp]),
             "fd_decode_host": (ctypes.c_int, [vp, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32, c_i32, f32, c_i32,
                                               vp, c_sz, vp]),
-            "fd_plan_pieces": (c_i64, [c_i32, c_i32, c_i32, vp, c_i32, c_i32, c_i32, vp, c_i64]),
+            "fd_plan_pieces": (c_i64, [c_i32, c_i32, c_i32, c_i32, vp, c_i32, c_i32, c_i32, vp, c_i64]),
             "fd_decode_static": (ctypes.c_int, [vp, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32, c_i32, f32,
                                                 c_i32, vp]),
             "fd_decode_rows": (ctypes.c_int, [vp, c_i32, c_i32, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32,
@@ -119,16 +119,18 @@ def split_size(max_seq_len: int, n_splits: int) -> int:
     return int(_lib().fd_split_size(max_seq_len, n_splits))
 
 
-def plan_pieces(B, Hq, Hkv, seq_lens: Optional[Sequence[int]], max_seq_len, n_splits=0, grid=152) -> np.ndarray:
+def plan_pieces(B, Hq, Hkv, seq_lens: Optional[Sequence[int]], max_seq_len, n_splits=0, grid=152,
+                kv_dtype="bf16") -> np.ndarray:
     """The pieces fd_decode runs: int32 [n, 7] of (cta, b, vkv, tok_begin, tok_end, slot, pieces_of_sequence)."""
     lib = _lib()
+    dt = {"bf16": FD_BF16, "f32": FD_F32}[kv_dtype]
     lens = None if seq_lens is None else np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
     lp = None if lens is None else lens.ctypes.data
-    n = lib.fd_plan_pieces(B, Hq, Hkv, lp, max_seq_len, n_splits, grid, None, 0)
+    n = lib.fd_plan_pieces(B, Hq, Hkv, dt, lp, max_seq_len, n_splits, grid, None, 0)
     if n < 0:
         raise FdError(FD_ERR_INVALID_ARG, "fd_plan_pieces")
     buf = np.zeros((max(n, 1), 7), dtype=np.int32)
-    lib.fd_plan_pieces(B, Hq, Hkv, lp, max_seq_len, n_splits, grid, buf.ctypes.data, n)
+    lib.fd_plan_pieces(B, Hq, Hkv, dt, lp, max_seq_len, n_splits, grid, buf.ctypes.data, n)
     return buf[:n]
 
 

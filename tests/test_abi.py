@@ -142,11 +142,12 @@ def test_binding_refuses_cpu_tensors(lib):
 
 
 # ------------------------------------------------------------------ planner
-def _check_balanced(B, Hq, Hkv, lens, max_len, grid):
-    pieces = fd.plan_pieces(B, Hq, Hkv, lens, max_len, 0, grid)
+def _check_balanced(B, Hq, Hkv, lens, max_len, grid, kv_dtype="bf16"):
+    pieces = fd.plan_pieces(B, Hq, Hkv, lens, max_len, 0, grid, kv_dtype=kv_dtype)
     g = Hq // Hkv
+    cap = 16 if kv_dtype == "bf16" else 8  # query heads one CTA serves from one K/V read
     gpad = 1
-    while gpad < g and gpad < 8:
+    while gpad < g and gpad < cap:
         gpad *= 2
     nsub = -(-g // gpad)
     hv = Hkv * nsub
@@ -191,7 +192,7 @@ def test_balanced_plan_random(lib, seed):
     lens = r.integers(0, max_len + 1, size=B)
     lens[r.integers(0, B)] = 0
     grid = int(r.choice([1, 7, 148, 152, 300]))
-    _check_balanced(B, g * Hkv, Hkv, lens.tolist(), max_len, grid)
+    _check_balanced(B, g * Hkv, Hkv, lens.tolist(), max_len, grid, kv_dtype=["bf16", "f32"][seed % 2])
 
 
 def test_balanced_plan_workloads(lib):
@@ -202,6 +203,16 @@ def test_balanced_plan_workloads(lib):
     lens = np.clip(np.floor(np.exp(r.uniform(np.log(512), np.log(65536), 64))), 512, 65536).astype(int)
     _check_balanced(64, 64, 8, lens.tolist(), 65536, 152)
     _check_balanced(3, 4, 4, [0, 0, 0], 100, 152)   # nothing to do
+    _check_balanced(4, 64, 2, [5000, 1, 300, 129], 5000, 152, kv_dtype="f32")  # g = 32: four sub-groups of 8
+    _check_balanced(4, 64, 2, [5000, 1, 300, 129], 5000, 152)                  # ... two of 16 for bf16
+
+
+def test_group_cap_follows_the_cache_dtype(lib):
+    # g = 16: one virtual KV head per KV head for bf16 (tensor-core engine), two for fp32
+    bf = fd.plan_pieces(1, 32, 2, None, 256, 1, kv_dtype="bf16")
+    f32 = fd.plan_pieces(1, 32, 2, None, 256, 1, kv_dtype="f32")
+    assert sorted(set(bf[:, 2].tolist())) == [0, 1]
+    assert sorted(set(f32[:, 2].tolist())) == [0, 1, 2, 3]
 
 
 def test_explicit_plan(lib):

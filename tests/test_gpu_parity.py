@@ -68,6 +68,10 @@ SMALL = [
     small_spec("peaked_q", 1, 4, 4, 128, 900, q_gain=6.0),
     small_spec("peaked_q_gqa8", 2, 16, 2, 128, 900, q_gain=6.0, lengths="uniform:1:900"),
     small_spec("gqa8_bf16_d64_ragged", 3, 16, 2, 64, 777, lengths="uniform:1:777"),
+    small_spec("gqa16_paged16", 3, 32, 2, 128, 650, layout="paged", page_size=16, lengths="uniform:1:650"),
+    small_spec("gqa32_bf16_two_subgroups", 2, 64, 2, 128, 300, lengths="uniform:1:300"),
+    small_spec("gqa16_f32_two_subgroups", 2, 32, 2, 64, 300, kv_dtype="f32", lengths="uniform:1:300"),
+    small_spec("peaked_q_gqa16", 2, 32, 2, 128, 900, q_gain=6.0, lengths="uniform:1:900"),
 ]
 
 
@@ -88,7 +92,7 @@ EDGE_LENGTHS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 127, 128, 129, 255, 256, 257, 1
 
 @pytest.mark.parametrize("layout,page", [("contiguous", 16), ("paged", 16), ("paged", 48)])
 @pytest.mark.parametrize("n_splits", [0, 2, 5])
-@pytest.mark.parametrize("hq", [8, 16])  # GQA groups of 4 (CUDA-core engine) and 8 (tensor-core engine)
+@pytest.mark.parametrize("hq", [8, 16, 32, 24])  # groups of 4, 8, 16 (tensor cores) and 12 (16 padded)
 def test_edge_lengths(layout, page, n_splits, hq):
     spec = small_spec(f"edges_{layout}{page}", len(EDGE_LENGTHS), hq, 2, 128, 1024, layout=layout, page_size=page,
                       seed=11)
@@ -149,7 +153,7 @@ def test_config5_paged_sampled():
 
 @pytest.mark.parametrize("layout", ["contiguous", "paged"])
 @pytest.mark.parametrize("n_splits", [0, 3])
-@pytest.mark.parametrize("hq,d", [(8, 128), (16, 128), (16, 64)])
+@pytest.mark.parametrize("hq,d", [(8, 128), (16, 128), (16, 64), (32, 128), (64, 64)])
 def test_masked_positions_are_bit_exact(layout, n_splits, hq, d):
     spec = small_spec(f"mask_{layout}", 6, hq, 2, d, 700, layout=layout, lengths="uniform:1:700", seed=21)
     case = make_case(spec, "cuda")

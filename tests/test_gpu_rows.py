@@ -40,17 +40,20 @@ def run_rows(case, q, causal, n_splits=0, **kw):
                           block_table=case.block_table, scale=case.spec.scale, n_splits=n_splits, **kw)
 
 
-# (spec, n_q): the virtual group g * n_q picks the engine: bf16 with g * n_q >= 4 runs on tensor cores
+# (spec, n_q): the virtual group g * n_q picks the engine: bf16 with g * n_q >= 4 runs on tensor cores,
+# more than 8 on the sixteen-head one
 SPECS = [
     (small_spec("mha_bf16_d128", 2, 4, 4, 128, 700, lengths="uniform:1:700"), 2),   # g'=2, CUDA cores
     (small_spec("mha_bf16_d128_q4", 2, 4, 4, 128, 700, lengths="uniform:1:700"), 4),  # g'=4, tensor cores
     (small_spec("gqa4_bf16_d128", 3, 16, 4, 128, 1000, lengths="uniform:1:1000"), 2),  # g'=8
-    (small_spec("gqa4_bf16_d64", 2, 8, 2, 64, 400, lengths="uniform:1:400"), 3),    # g'=12, ragged group
-    (small_spec("gqa8_bf16_d128", 2, 16, 2, 128, 500), 2),                          # g'=16, two sub-groups
+    (small_spec("gqa4_bf16_d64", 2, 8, 2, 64, 400, lengths="uniform:1:400"), 3),    # g'=12 of 16 rows
+    (small_spec("gqa8_bf16_d128", 2, 16, 2, 128, 500), 2),                          # g'=16, sixteen-head engine
     (small_spec("mha_f32_d64", 2, 4, 4, 64, 513, kv_dtype="f32"), 3),               # fp32 cache
     (small_spec("paged16_gqa2", 3, 8, 4, 128, 600, layout="paged", page_size=16, lengths="uniform:1:600"), 4),
     (small_spec("paged32_mha_f32", 2, 2, 2, 64, 300, kv_dtype="f32", layout="paged", page_size=32,
                 lengths="uniform:1:300"), 2),
+    (small_spec("paged16_gqa8", 3, 16, 2, 128, 700, layout="paged", page_size=16, lengths="uniform:1:700"), 2),
+    (small_spec("gqa8_rows4", 2, 16, 2, 128, 400, lengths="uniform:1:400"), 4),     # g'=32, two groups of 16
 ]
 
 
@@ -67,7 +70,7 @@ def test_rows_vs_oracle(spec, n_q, causal, n_splits):
     assert_close(np64(lse), ref_lse, "lse")
 
 
-@pytest.mark.parametrize("hq,n_q", [(4, 4), (8, 2), (16, 3)])
+@pytest.mark.parametrize("hq,n_q", [(4, 4), (8, 2), (16, 2), (16, 3)])
 @pytest.mark.parametrize("layout", ["contiguous", "paged"])
 @pytest.mark.parametrize("n_splits", [0, 2])
 def test_rows_shorter_than_the_window(hq, n_q, layout, n_splits):
@@ -86,7 +89,7 @@ def test_rows_shorter_than_the_window(hq, n_q, layout, n_splits):
 
 
 @pytest.mark.parametrize("layout", ["contiguous", "paged"])
-@pytest.mark.parametrize("hq,n_q", [(4, 2), (8, 4)])
+@pytest.mark.parametrize("hq,n_q", [(4, 2), (8, 4), (8, 8)])
 def test_rows_masked_positions_are_bit_exact(layout, hq, n_q):
     spec = small_spec("poison", 3, hq, 4, 128, 400, layout=layout, lengths="uniform:1:400")
     case = make_case(spec, "cuda")
