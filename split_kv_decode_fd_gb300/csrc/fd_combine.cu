@@ -12,10 +12,12 @@ __global__ void __launch_bounds__(128) fd_combine_kernel(const float* __restrict
                                                          const float* __restrict__ m_part,
                                                          const float* __restrict__ l_part, float* out,
                                                          float* lse, int BH, int n_splits) {
+  __shared__ __align__(16) float wsm[4][128];
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= BH) return;
-  merge_head<D>(o_part, m_part, l_part, (size_t)row * n_splits, 1, n_splits, out + (size_t)row * D,
-                lse ? lse + row : nullptr, threadIdx.x & 31);
+  const GlobalPartials<D> src{o_part, m_part, l_part, (size_t)row * n_splits, 1};
+  merge_head<D>(src, n_splits, out + (size_t)row * D, lse ? lse + row : nullptr, threadIdx.x & 31,
+                wsm[threadIdx.x >> 5]);
 }
 
 cudaError_t launch_combine(int D, const float* o_part, const float* m_part, const float* l_part, float* out,

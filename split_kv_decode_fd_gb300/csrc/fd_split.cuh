@@ -123,7 +123,9 @@ struct SplitCfg {
   static constexpr int kUOff = kQOff + kQBufs * kQBytes;
   static constexpr int kPBytes = kMma ? 0 : kWarps * 32 * G * 8;  // CUDA-core engine's p rows
   static constexpr int kObBytes = kWarps * kPubHeads * D * 4;
-  static constexpr int kUBytes = kPBytes > kObBytes ? kPBytes : kObBytes;
+  static constexpr int kWsBytes = kWarps * 128 * 4;  // merge_head weight scratch (fused merge)
+  static constexpr int kUBytes0 = kPBytes > kObBytes ? kPBytes : kObBytes;
+  static constexpr int kUBytes = kUBytes0 > kWsBytes ? kUBytes0 : kWsBytes;
   static constexpr int kMlOff = kUOff + kUBytes;
   static constexpr int kFinOff = kMlOff + kWarps * kPubHeads * 8;
   static constexpr int kLenOff = kFinOff + kPubHeads * 8;
@@ -159,12 +161,15 @@ struct CtaTiles {
 };
 
 // Log-sum-exp merge of `count` split states of one head (the combine
-// walkthrough), by one warp.  Split k lives at o + (base + k*stride)*D and
-// m/l + base + k*stride.  The loads are issued in batches so that the merge
-// costs a few L2 round trips rather than one per split.  Summation order is
-// fixed: per output element, four partial sums over k = 0, 1, 2, 3 (mod 4) in
-// increasing k, then ((s0 + s1) + s2) + s3 -- bit-reproducible, and the same
-// for the fused merge and fd_combine.
+// walkthrough), by one warp.  The states come from a partials source P:
+// P::m(k), P::l(k) and P::slice(k, lane, v) (this lane's D/32 elements of
+// O_k); GlobalPartials reads them from the workspace (L2).  `wsm` is the
+// warp's scratch of 128 floats in shared memory (16-byte aligned).  The loads are issued in
+// batches so that the merge costs a few round trips rather than one per
+// split.  Summation order is fixed: per output element, four partial sums
+// over k = 0, 1, 2, 3 (mod 4) in increasing k, then ((s0 + s1) + s2) + s3 --
+// bit-reproducible, and the same in the fused merge and in fd_combine, which
+// therefore give identical bits.
 template <int D>
 __device__ __forceinline__ void load_slice(const float* row, float (&v)[D / 32]) {
   if constexpr (D / 32 == 4) {
@@ -180,14 +185,24 @@ __device__ __forceinline__ void load_slice(const float* row, float (&v)[D / 32])
   }
 }
 
+// Split k of one head at o + (base + k*stride)*D, m/l + base + k*stride.
 template <int D>
-__device__ __forceinline__ void merge_head(const float* o, const float* m, const float* l, size_t base,
-                                           size_t stride, int count, float* out_row, float* lse_slot,
-                                           int lane) {
+struct GlobalPartials {
+  const float *o, *m_, *l_;
+  size_t base, stride;
+  __device__ __forceinline__ float m(int k) const { return __ldcg(m_ + base + (size_t)k * stride); }
+  __device__ __forceinline__ float l(int k) const { return __ldcg(l_ + base + (size_t)k * stride); }
+  __device__ __forceinline__ void slice(int k, int lane, float (&v)[D / 32]) const {
+    load_slice<D>(o + (base + (size_t)k * stride) * D + lane * (D / 32), v);
+  }
+};
+
+template <int D, class P>
+__device__ __forceinline__ void merge_head(const P& src, int count, float* out_row, float* lse_slot, int lane,
+                                           float* wsm) {
   constexpr int EPL = D / 32;
   constexpr int KR = 4;                 // splits per lane whose (m, l) stay in registers: count <= 128
   constexpr int NB = 128 / EPL;         // splits per batch of O loads (128 registers)
-  const float* src = o + base * D + lane * EPL;
   // Round trip 1: every (m, l) and the first batch of O slices, all in flight together.
   float mk[KR], lk[KR];
 #pragma unroll
@@ -196,9 +211,8 @@ __device__ __forceinline__ void merge_head(const float* o, const float* m, const
     mk[r] = -INFINITY;
     lk[r] = 0.f;
     if (k < count) {
-      const size_t i = base + (size_t)k * stride;
-      lk[r] = __ldcg(l + i);
-      mk[r] = __ldcg(m + i);
+      lk[r] = src.l(k);
+      mk[r] = src.m(k);
     }
   }
   float v[NB][EPL];
@@ -206,16 +220,14 @@ __device__ __forceinline__ void merge_head(const float* o, const float* m, const
   for (int j = 0; j < NB; ++j) {
 #pragma unroll
     for (int e = 0; e < EPL; ++e) v[j][e] = 0.f;
-    if (j < count) load_slice<D>(src + (size_t)j * stride * D, v[j]);
+    if (j < count) src.slice(j, lane, v[j]);
   }
   float mx = -INFINITY;
 #pragma unroll
   for (int r = 0; r < KR; ++r)
     if (lk[r] > 0.f) mx = fmaxf(mx, mk[r]);
-  for (int k = KR * 32 + lane; k < count; k += 32) {
-    const size_t i = base + (size_t)k * stride;
-    if (__ldcg(l + i) > 0.f) mx = fmaxf(mx, __ldcg(m + i));
-  }
+  for (int k = KR * 32 + lane; k < count; k += 32)
+    if (src.l(k) > 0.f) mx = fmaxf(mx, src.m(k));
   mx = warp_max(mx);
   if (mx == -INFINITY) {
 #pragma unroll
@@ -231,11 +243,15 @@ __device__ __forceinline__ void merge_head(const float* o, const float* m, const
     lsum = fmaf(wk[r], lk[r], lsum);
   }
   for (int k = KR * 32 + lane; k < count; k += 32) {
-    const size_t i = base + (size_t)k * stride;
-    const float lv = __ldcg(l + i);
-    if (lv > 0.f) lsum = fmaf(exp2f((__ldcg(m + i) - mx) * kLog2e), lv, lsum);
+    const float lv = src.l(k);
+    if (lv > 0.f) lsum = fmaf(exp2f((src.m(k) - mx) * kLog2e), lv, lsum);
   }
   const float L = warp_sum(lsum);
+  // weight of split k (< 128) at wsm[k]; 0 past `count` (there l = 0)
+  __syncwarp();  // the warp's reads of an earlier merge are done
+#pragma unroll
+  for (int r = 0; r < KR; ++r) wsm[r * 32 + lane] = wk[r];
+  __syncwarp();
   float acc[4][EPL];
 #pragma unroll
   for (int s4 = 0; s4 < 4; ++s4)
@@ -247,25 +263,36 @@ __device__ __forceinline__ void merge_head(const float* o, const float* m, const
       for (int j = 0; j < NB; ++j) {
 #pragma unroll
         for (int e = 0; e < EPL; ++e) v[j][e] = 0.f;
-        if (k0 + j < count) load_slice<D>(src + (size_t)(k0 + j) * stride * D, v[j]);
+        if (k0 + j < count) src.slice(k0 + j, lane, v[j]);
       }
     }
+    // Weights four splits per shared-memory load (the warp's scratch), the
+    // rest (count > 128) from the source.  Splits past `count` have w = 0 and
+    // v = 0, and fmaf(0, 0, a) == a: the padding leaves the sums' bits as they are.
 #pragma unroll
-    for (int j = 0; j < NB; ++j) {
-      const int k = k0 + j;
-      if (k >= count) break;  // warp-uniform
-      const int r = k >> 5;
-      float w;
-      if (r < KR) {
-        const float ws = r == 0 ? wk[0] : (r == 1 ? wk[1] : (r == 2 ? wk[2] : wk[3]));
-        w = __shfl_sync(0xffffffffu, ws, k & 31);
+    for (int j4 = 0; j4 < NB; j4 += 4) {
+      float w[4] = {0.f, 0.f, 0.f, 0.f};
+      if (k0 + j4 < KR * 32) {
+        const float4 x = *reinterpret_cast<const float4*>(wsm + k0 + j4);
+        w[0] = x.x;
+        w[1] = x.y;
+        w[2] = x.z;
+        w[3] = x.w;
       } else {
-        const size_t i = base + (size_t)k * stride;
-        const float lv = __ldcg(l + i);
-        w = lv > 0.f ? exp2f((__ldcg(m + i) - mx) * kLog2e) : 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int k = k0 + j4 + jj;
+          if (k < count) {
+            const float lv = src.l(k);
+            w[jj] = lv > 0.f ? exp2f((src.m(k) - mx) * kLog2e) : 0.f;
+          }
+        }
       }
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[j & 3][e] = fmaf(w, v[j][e], acc[j & 3][e]);
+      for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e)
+          acc[(j4 + jj) & 3][e] = fmaf(w[jj], v[j4 + jj][e], acc[(j4 + jj) & 3][e]);
     }
   }
 #pragma unroll
@@ -704,9 +731,10 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
 
     // Does this piece hold the whole sequence?  Then it is the output.
     int npieces = 1;
+    int32_t first = 0;  // balanced: first CTA holding this sequence
     const int32_t pair = pc.b * p.hv + pc.vkv;
     if (balanced) {
-      int32_t first, last;
+      int32_t last;
       balanced_pair_ctas(tl, p.hv, total, balanced_ctas(total, (int32_t)gridDim.x), pc.b, pc.vkv, &first,
                          &last);
       npieces = last - first + 1;
@@ -727,12 +755,13 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
 #pragma unroll
         for (int w = 0; w < W; ++w) M = fmaxf(M, mlbuf[(w * PH + tid) * 2]);
         float L = 0.f;
-        if (M != -INFINITY) {
 #pragma unroll
-          for (int w = 0; w < W; ++w) {
-            const float mw = mlbuf[(w * PH + tid) * 2];
-            if (mw != -INFINITY) L = fmaf(exp2f(mw - M), mlbuf[(w * PH + tid) * 2 + 1], L);
-          }
+        for (int w = 0; w < W; ++w) {
+          // each warp state's weight exp2(m_w - M), once per head (0 for an empty state)
+          const float mw = mlbuf[(w * PH + tid) * 2];
+          const float sw = mw == -INFINITY ? 0.f : exp2f(mw - M);
+          if (mw != -INFINITY) L = fmaf(sw, mlbuf[(w * PH + tid) * 2 + 1], L);
+          mlbuf[(w * PH + tid) * 2] = sw;
         }
         fin[tid * 2] = M;
         fin[tid * 2 + 1] = L;
@@ -744,14 +773,10 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
         const int h = r * PH + hl;
         if (h >= nh) continue;
         const float M = fin[hl * 2];
+        // an empty warp state has weight 0 and O = 0, and fmaf(0, 0, a) == a
         float acc = 0.f;
-        if (M != -INFINITY) {
 #pragma unroll
-          for (int w = 0; w < W; ++w) {
-            const float mw = mlbuf[(w * PH + hl) * 2];
-            if (mw != -INFINITY) acc = fmaf(exp2f(mw - M), obuf[(w * PH + hl) * D + d], acc);
-          }
-        }
+        for (int w = 0; w < W; ++w) acc = fmaf(mlbuf[(w * PH + hl) * 2], obuf[(w * PH + hl) * D + d], acc);
         if (final_here) {
           const float L = fin[hl * 2 + 1];
           p.out[((size_t)pc.b * p.Hq + head0 + h) * D + d] = M == -INFINITY ? 0.f : acc / L;
@@ -787,22 +812,20 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
         size_t base0, stride;
         int count;
         if (balanced) {
-          int32_t first, last;
-          balanced_pair_ctas(tl, p.hv, total, balanced_ctas(total, (int32_t)gridDim.x), pc.b, pc.vkv, &first,
-                         &last);
           base0 = (size_t)(pair + first) * G;
           stride = G;
-          count = last - first + 1;
+          count = npieces;
         } else {
           base0 = ((size_t)pc.b * p.Hq + head0) * p.n_splits;
           stride = 1;
           count = p.n_splits;
         }
+        // Head h, split k: state base0 + h*hs + k*stride.
+        const size_t hs = balanced ? 1 : (size_t)p.n_splits;
         for (int h = warp; h < nh; h += W) {
-          const size_t base = balanced ? base0 + h : base0 + (size_t)h * p.n_splits;
-          merge_head<D>(p.o_part, p.m_part, p.l_part, base, stride, count,
-                        p.out + ((size_t)pc.b * p.Hq + head0 + h) * D,
-                        p.lse ? p.lse + (size_t)pc.b * p.Hq + head0 + h : nullptr, lane);
+          const GlobalPartials<D> src{p.o_part, p.m_part, p.l_part, base0 + h * hs, stride};
+          merge_head<D>(src, count, p.out + ((size_t)pc.b * p.Hq + head0 + h) * D,
+                        p.lse ? p.lse + (size_t)pc.b * p.Hq + head0 + h : nullptr, lane, obuf + warp * 128);
         }
         if (tid == 0) p.counters[pair] = 0;  // ready for the next call
       }
