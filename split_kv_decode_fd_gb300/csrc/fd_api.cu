@@ -100,6 +100,7 @@ fd_status check_kv(const fd_kv_desc* kv, int B, int Hkv, int max_seq_len) {
         kv->max_pages_per_seq < 1)
       return FD_ERR_INVALID_ARG;
     if ((int64_t)kv->max_pages_per_seq * kv->page_size < max_seq_len) return FD_ERR_INVALID_ARG;
+    if ((int64_t)kv->num_pages * Hkv > INT32_MAX) return FD_ERR_UNSUPPORTED;  // TMA row-block coordinate
   } else {
     return FD_ERR_INVALID_ARG;
   }
@@ -128,8 +129,8 @@ fd_status make_maps(const fd_kv_desc* kv, int B, int Hkv, int D, CUtensorMap* tk
   const CUtensorMapDataType dt =
       kv->dtype == FD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const cuuint64_t es = kv->dtype == FD_BF16 ? 2 : 4;
-  cuuint64_t dims[4], strides[3];
-  cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3], estr[3] = {1, 1, 1};
   cuuint32_t rank;
   if (kv->layout == FD_KV_CONTIGUOUS) {
     rank = 3;
@@ -142,18 +143,17 @@ fd_status make_maps(const fd_kv_desc* kv, int B, int Hkv, int D, CUtensorMap* tk
     box[1] = 16;
     box[2] = 1;
   } else {
-    rank = 4;
+    // the pool [num_pages, Hkv, page_size, D] as [num_pages * Hkv, page_size, D]
+    // (measured faster than the 4-D view of the same boxes)
+    rank = 3;
     dims[0] = (cuuint64_t)D;
     dims[1] = (cuuint64_t)kv->page_size;
-    dims[2] = (cuuint64_t)Hkv;
-    dims[3] = (cuuint64_t)kv->num_pages;
+    dims[2] = (cuuint64_t)kv->num_pages * Hkv;
     strides[0] = (cuuint64_t)D * es;
     strides[1] = (cuuint64_t)kv->page_size * D * es;
-    strides[2] = (cuuint64_t)Hkv * kv->page_size * D * es;
     box[0] = (cuuint32_t)(128 / es);
     box[1] = 16;
     box[2] = 1;
-    box[3] = 1;
   }
   const void* ptrs[2] = {kv->k, kv->v};
   CUtensorMap* maps[2] = {tk, tv};

@@ -359,6 +359,11 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
   gr.nsub = p.nsub;
   gr.hv = p.hv;
 
+  constexpr int kPageAhead = 4;
+  // one tile advances a lane's position by step_q pages and step_r rows
+  const int32_t step_q = p.paged ? C::kBT / p.page_size : 0;
+  const int32_t step_r = p.paged ? C::kBT % p.page_size : 0;
+
   PieceIter pieces(p, tl, total);
   Piece pc;
   while (pieces.next(pc)) {
@@ -379,55 +384,81 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
     }
     ++qi;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    // Paged: lane j looks up the page of row block j of a tile one tile ahead, so
-    // the table load overlaps the wait for a free stage.  Only entries of keys
-    // below tok_end (<= L_b) are ever read.
+    // Paged: lane j looks up the page of row block j of a tile kPageAhead tiles
+    // ahead, so the table loads -- which miss L2 once the K/V stream has
+    // evicted the table -- overlap several stages.  The tile loop is unrolled
+    // by kPageAhead so that each queue slot stays in its own register (moving
+    // a register would wait for its load).  Positions advance by a fixed
+    // (pages, rows) step per tile: no division in the loop.  Only entries of
+    // keys below tok_end (<= L_b) are ever read.
     const int32_t* trow = p.paged ? p.block_table + (size_t)pc.b * p.max_pages : nullptr;
-    int32_t page_next = 0;
-    if (p.paged && pc.tok_begin + 16 * lane < pc.tok_end)
-      page_next = __ldg(trow + (pc.tok_begin + 16 * lane) / p.page_size);
-    for (int32_t t0 = pc.tok_begin; ok && t0 < pc.tok_end; t0 += C::kBT, ++it) {
-      const int32_t nvalid = pc.tok_end - t0 < C::kBT ? pc.tok_end - t0 : C::kBT;
-      const int32_t nbox = ceil_div(nvalid, 16);
-      int32_t page = page_next;
-      bool mine = lane < nbox;
-      if (p.paged) {
-        const int32_t tn = t0 + C::kBT + 16 * lane;
-        if (tn < pc.tok_end) page_next = __ldg(trow + tn / p.page_size);
-        if (mine && (page < 0 || page >= p.num_pages)) {
-          raise_error(p.err, kErrBadIndex);
-          mine = false;
-        }
-      }
-      const unsigned issue = __ballot_sync(0xffffffffu, mine);
-      const uint32_t stage = it % C::kStages;
-      const uint32_t phase = (it / C::kStages) & 1;
-      if (lane == 0) {
-        if (*abort_flag || !mbar_wait(empty + stage, phase ^ 1)) {
-          ok = false;
-        } else {
-          mbar_arrive_expect_tx(full + stage, (uint32_t)__popc(issue) * C::kNB * 2 * C::kBoxBytes);
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (mine) {
-        uint8_t* kdst = smem + stage * C::kStageBytes + lane * C::kBoxBytes;
-        uint8_t* vdst = kdst + C::kTileBytes;
+    int32_t pq[kPageAhead];
+    int32_t cur_row = 0, a_tn = 0, a_idx = 0, a_row = 0;
+    if (p.paged) {
+      const int32_t tn0 = pc.tok_begin + 16 * lane;
 #pragma unroll
-        for (int nb = 0; nb < C::kNB; ++nb) {
-          const int32_t x = nb * (128 / C::kEs);
-          const int32_t off = nb * C::kBT * 128;
-          if (p.paged) {
-            const int32_t row = (t0 + 16 * lane) % p.page_size;
-            tma_load_4d(kdst + off, tk, full + stage, x, row, kvh, page);
-            tma_load_4d(vdst + off, tv, full + stage, x, row, kvh, page);
-          } else {
-            const int32_t z = pc.b * p.Hkv + kvh;
-            tma_load_3d(kdst + off, tk, full + stage, x, t0 + 16 * lane, z);
-            tma_load_3d(vdst + off, tv, full + stage, x, t0 + 16 * lane, z);
+      for (int a = 0; a < kPageAhead; ++a) {
+        const int32_t tn = tn0 + a * C::kBT;
+        pq[a] = tn < pc.tok_end ? __ldg(trow + tn / p.page_size) : 0;
+      }
+      cur_row = tn0 % p.page_size;
+      a_tn = tn0 + kPageAhead * C::kBT;
+      a_idx = a_tn / p.page_size;
+      a_row = a_tn - a_idx * p.page_size;
+    }
+    for (int32_t t0 = pc.tok_begin; ok && t0 < pc.tok_end;) {
+#pragma unroll
+      for (int slot = 0; slot < kPageAhead; ++slot) {
+        if (!ok || t0 >= pc.tok_end) break;
+        const int32_t nvalid = pc.tok_end - t0 < C::kBT ? pc.tok_end - t0 : C::kBT;
+        const int32_t nbox = ceil_div(nvalid, 16);
+        bool mine = lane < nbox;
+        int32_t page = 0, row = t0 + 16 * lane;
+        if (p.paged) {
+          page = pq[slot];
+          row = cur_row;
+          cur_row += step_r;
+          if (cur_row >= p.page_size) cur_row -= p.page_size;
+          pq[slot] = a_tn < pc.tok_end ? __ldg(trow + a_idx) : 0;
+          a_tn += C::kBT;
+          a_idx += step_q;
+          a_row += step_r;
+          if (a_row >= p.page_size) {
+            a_row -= p.page_size;
+            ++a_idx;
+          }
+          if (mine && (page < 0 || page >= p.num_pages)) {
+            raise_error(p.err, kErrBadIndex);
+            mine = false;
           }
         }
+        const unsigned issue = __ballot_sync(0xffffffffu, mine);
+        const uint32_t stage = it % C::kStages;
+        const uint32_t phase = (it / C::kStages) & 1;
+        if (lane == 0) {
+          if (*abort_flag || !mbar_wait(empty + stage, phase ^ 1)) {
+            ok = false;
+          } else {
+            mbar_arrive_expect_tx(full + stage, (uint32_t)__popc(issue) * C::kNB * 2 * C::kBoxBytes);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (mine) {
+          uint8_t* kdst = smem + stage * C::kStageBytes + lane * C::kBoxBytes;
+          uint8_t* vdst = kdst + C::kTileBytes;
+          // paged pool viewed as [num_pages * Hkv, page_size, D]; contiguous [B * Hkv, T_cap, D]
+          const int32_t z = p.paged ? page * p.Hkv + kvh : pc.b * p.Hkv + kvh;
+#pragma unroll
+          for (int nb = 0; nb < C::kNB; ++nb) {
+            const int32_t x = nb * (128 / C::kEs);
+            const int32_t off = nb * C::kBT * 128;
+            tma_load_3d(kdst + off, tk, full + stage, x, row, z);
+            tma_load_3d(vdst + off, tv, full + stage, x, row, z);
+          }
+        }
+        t0 += C::kBT;
+        ++it;
       }
     }
   }
