@@ -42,10 +42,15 @@ Readings taken where the pages are silent:
   ``t % page_size``.
 * Explicit split size: ``S = 16 * ceil(ceil(max_seq_len / n_splits) / 16)``;
   split ``s`` covers tokens ``[s*S, min((s+1)*S, L_b))``.
-* Several query rows per sequence ("FlashDecoding and split-KV": one query row,
-  or a small batch of them): the ``n_q`` new tokens are the last ``n_q`` keys of
-  the cache; with causal masking row ``i`` attends keys ``t < L_b - (n_q-1-i)``,
-  without it every row attends all ``L_b`` keys.
+* Several query rows per sequence ("FlashDecoding and split-KV", "Walking
+  through it", lets decode carry a few query rows): the ``n_q`` new tokens are
+  the last ``n_q`` keys of the cache; with causal masking row ``i`` attends keys
+  ``t < L_b - (n_q-1-i)``, without it every row attends all ``L_b`` keys.
+* Fused append-KV (named on the same page, not specified): the new token's key
+  and value (already in the cache's dtype) are written at position ``L_b`` of
+  sequence ``b`` -- contiguous row ``L_b``, or row ``L_b % page_size`` of page
+  ``block_table[b, L_b // page_size]`` -- and the decode then attends the
+  ``L_b + 1`` keys.  The lengths passed in are the lengths before the append.
 
 All arithmetic is float64.  Inputs are widened exactly (bf16 and fp32 values are
 exactly representable in float64); ``scale`` is taken as given.
@@ -70,6 +75,8 @@ __all__ = [
     "split_partials",
     "row_key_limit",
     "decode_rows",
+    "append_kv",
+    "append_decode",
 ]
 
 
@@ -310,3 +317,45 @@ def decode_rows(q, k, v, scale, causal=True, seq_lens=None, max_seq_len=None, bl
                     lim = row_key_limit(lens[b], n_q, i, causal)
                     out[b, h, i], lse[b, h, i] = attend_row(q[b, h, i], k_rows[:lim], v_rows[:lim], scale)
     return out, lse
+
+
+def append_kv(k, v, k_new, v_new, seq_lens=None, max_seq_len=None, block_table=None, page_size=None):
+    """Caches after writing one new token per (b, KV head) at position ``L_b``.
+
+    ``k_new``, ``v_new``: ``[B, Hkv, D]``.  Returns float64 copies of ``k`` and
+    ``v`` in which only the rows at position ``L_b`` (per sequence and KV head)
+    differ from the input.
+    """
+    k2, v2 = _f64(k).copy(), _f64(v).copy()
+    k_new, v_new = _f64(k_new), _f64(v_new)
+    batch, hkv = k_new.shape[0], k_new.shape[1]
+    if block_table is None and max_seq_len is None:
+        max_seq_len = np.shape(k)[2] - 1
+    lens = _lengths(seq_lens, batch, max_seq_len)
+    for b in range(batch):
+        t = lens[b]
+        for kvh in range(hkv):
+            if block_table is None:
+                k2[b, kvh, t] = k_new[b, kvh]
+                v2[b, kvh, t] = v_new[b, kvh]
+            else:
+                page = int(block_table[b][t // page_size])
+                k2[page, kvh, t % page_size] = k_new[b, kvh]
+                v2[page, kvh, t % page_size] = v_new[b, kvh]
+    return k2, v2
+
+
+def append_decode(q, k, v, k_new, v_new, scale, seq_lens=None, max_seq_len=None, block_table=None,
+                  page_size=None):
+    """Fused append-KV + decode: :func:`append_kv`, then :func:`decode` over ``L_b + 1`` keys.
+
+    Returns ``(out, lse, k_after, v_after)``.
+    """
+    batch = np.shape(q)[0]
+    if block_table is None and max_seq_len is None:
+        max_seq_len = np.shape(k)[2] - 1
+    lens = _lengths(seq_lens, batch, max_seq_len)
+    k2, v2 = append_kv(k, v, k_new, v_new, lens, max_seq_len, block_table, page_size)
+    out, lse = decode(q, k2, v2, scale, seq_lens=[x + 1 for x in lens], max_seq_len=max_seq_len + 1,
+                      block_table=block_table, page_size=page_size)
+    return out, lse, k2, v2

@@ -382,6 +382,90 @@ def check_rows_reduce_to_single_row():
     assert oracle.row_key_limit(2, 4, 2, True) == 1 and oracle.row_key_limit(2, 4, 0, False) == 2
 
 
+def _gather_rows(cache, b, kvh, n, table=None, page=None):
+    """First n rows of (b, kvh), gathered here with its own indexing (not the oracle's)."""
+    cache = np.asarray(cache, dtype=np.float64)
+    if table is None:
+        return cache[b, kvh, :n]
+    return np.stack([cache[int(table[b][t // page]), kvh, t % page] for t in range(n)]) if n else \
+        np.zeros((0, cache.shape[-1]))
+
+
+def check_append_decode_against_sdpa():
+    """Fused append + decode equals SDPA (float64) over the old keys followed by the new one."""
+    import torch
+    import torch.nn.functional as F
+    for paged in (False, True):
+        r = _rng(77 + paged)
+        B, Hq, Hkv, D, page = 3, 6, 2, 8, 4
+        lens = [0, 5, 11]
+        if paged:
+            npg = [-(-(L + 1) // page) for L in lens]
+            perm = r.permutation(sum(npg) + 2)
+            table = np.full((B, 4), -1)
+            c = 0
+            for b, n in enumerate(npg):
+                table[b, :n] = perm[c:c + n]
+                c += n
+            k = r.standard_normal((sum(npg) + 2, Hkv, page, D))
+            v = r.standard_normal((sum(npg) + 2, Hkv, page, D))
+            kw = dict(block_table=table, page_size=page, max_seq_len=max(lens))
+        else:
+            table = None
+            k = r.standard_normal((B, Hkv, 12, D))
+            v = r.standard_normal((B, Hkv, 12, D))
+            kw = dict(max_seq_len=max(lens))
+        q = r.standard_normal((B, Hq, D))
+        k_new = r.standard_normal((B, Hkv, D))
+        v_new = r.standard_normal((B, Hkv, D))
+        out, lse, _, _ = oracle.append_decode(q, k, v, k_new, v_new, 0.4, seq_lens=lens, **kw)
+        g = Hq // Hkv
+        for b in range(B):
+            L = lens[b]
+            ks = np.stack([np.concatenate([_gather_rows(k, b, j, L, table, page), k_new[b, j][None]]) for j in range(Hkv)])
+            vs = np.stack([np.concatenate([_gather_rows(v, b, j, L, table, page), v_new[b, j][None]]) for j in range(Hkv)])
+            kt = torch.from_numpy(ks[None]).repeat_interleave(g, dim=1)
+            vt = torch.from_numpy(vs[None]).repeat_interleave(g, dim=1)
+            qt = torch.from_numpy(q[b][None, :, None, :])
+            ref = F.scaled_dot_product_attention(qt, kt, vt, scale=0.4)[0, :, 0].numpy()
+            np.testing.assert_allclose(out[b], ref, rtol=0, atol=1e-13)
+            s = 0.4 * np.einsum("hd,htd->ht", q[b], kt[0].numpy())
+            np.testing.assert_allclose(lse[b], np.log(np.exp(s).sum(-1)), rtol=0, atol=1e-12)
+        # the empty sequence sees only the new key: out = v_new, lse = scale * q . k_new
+        np.testing.assert_array_equal(out[0], np.repeat(v_new[0], g, axis=0))
+
+
+def check_append_writes_one_row():
+    """The append changes exactly the row at position L_b of every (b, KV head), to the new values."""
+    for paged in (False, True):
+        r = _rng(91 + paged)
+        B, Hkv, D, page = 2, 3, 4, 4
+        lens = [3, 8]
+        if paged:
+            table = np.array([[5, 1, 7], [2, 6, 0]])
+            k = r.standard_normal((9, Hkv, page, D))
+            v = r.standard_normal((9, Hkv, page, D))
+            kw = dict(block_table=table, page_size=page, max_seq_len=8)
+            where = {0: (5, 3), 1: (0, 0)}  # L=3: page table[0][0]=5, row 3; L=8: page table[1][2]=0, row 0
+        else:
+            k = r.standard_normal((B, Hkv, 10, D))
+            v = r.standard_normal((B, Hkv, 10, D))
+            kw = dict(max_seq_len=8)
+        k_new = r.standard_normal((B, Hkv, D))
+        v_new = r.standard_normal((B, Hkv, D))
+        k2, v2 = oracle.append_kv(k, v, k_new, v_new, seq_lens=lens, **kw)
+        changed = np.argwhere(np.any(k2 != k, axis=-1))
+        expect = []
+        for b in range(B):
+            for j in range(Hkv):
+                expect.append((where[b][0], j, where[b][1]) if paged else (b, j, lens[b]))
+                idx = expect[-1]
+                np.testing.assert_array_equal(k2[idx], k_new[b, j])
+                np.testing.assert_array_equal(v2[idx], v_new[b, j])
+        assert sorted(map(tuple, changed.tolist())) == sorted(expect)
+        assert np.count_nonzero(np.any(v2 != v, axis=-1)) == len(expect)
+
+
 ALL_CHECKS = [
     check_single_key,
     check_identical_keys_mean,
@@ -398,6 +482,8 @@ ALL_CHECKS = [
     check_paged_matches_gather,
     check_rows_against_sdpa_with_mask,
     check_rows_reduce_to_single_row,
+    check_append_decode_against_sdpa,
+    check_append_writes_one_row,
 ]
 
 

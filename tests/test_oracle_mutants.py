@@ -126,7 +126,37 @@ def _mut_row_limit_off_by_one(length, n_q, row, causal):
     return max(0, min(lim, length))
 
 
+def _mut_append_one_early(k, v, k_new, v_new, seq_lens=None, max_seq_len=None, block_table=None, page_size=None):
+    lens = [max(0, int(x) - 1) for x in np.asarray(seq_lens).reshape(-1)]  # writes over the last old key
+    return fo.__dict__["_orig_append_kv"](k, v, k_new, v_new, lens, max_seq_len, block_table, page_size)
+
+
+def _mut_append_page_row_swapped(k, v, k_new, v_new, seq_lens=None, max_seq_len=None, block_table=None,
+                                 page_size=None):
+    if block_table is None:
+        return fo.__dict__["_orig_append_kv"](k, v, k_new, v_new, seq_lens, max_seq_len, block_table, page_size)
+    k2, v2 = np.asarray(k, dtype=np.float64).copy(), np.asarray(v, dtype=np.float64).copy()
+    for b, t in enumerate(np.asarray(seq_lens).reshape(-1)):
+        page = int(block_table[b][t % page_size]) if t % page_size < len(block_table[b]) else 0
+        for j in range(k2.shape[1]):
+            k2[max(page, 0), j, t // page_size % page_size] = k_new[b, j]
+            v2[max(page, 0), j, t // page_size % page_size] = v_new[b, j]
+    return k2, v2
+
+
+def _mut_append_decode_skips_new_key(q, k, v, k_new, v_new, scale, seq_lens=None, max_seq_len=None,
+                                     block_table=None, page_size=None):
+    lens = [int(x) for x in np.asarray(seq_lens).reshape(-1)]
+    k2, v2 = fo.append_kv(k, v, k_new, v_new, lens, max_seq_len, block_table, page_size)
+    out, lse = fo.decode(q, k2, v2, scale, seq_lens=lens, max_seq_len=max_seq_len, block_table=block_table,
+                         page_size=page_size)
+    return out, lse, k2, v2
+
+
 MUTANTS = {
+    "append_one_early": {"append_kv": _mut_append_one_early},
+    "append_page_row_swapped": {"append_kv": _mut_append_page_row_swapped},
+    "append_decode_skips_new_key": {"append_decode": _mut_append_decode_skips_new_key},
     "row_limit_off_by_one": {"row_key_limit": _mut_row_limit_off_by_one},
     "head_map_modulo": {"kv_head_for": _mut_head_map},
     "scale_dropped": {"scores": _mut_no_scale},
@@ -166,6 +196,7 @@ def test_unmutated_oracle_passes_every_pin():
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_mutant(name, monkeypatch):
     monkeypatch.setitem(fo.__dict__, "_orig_sequence_rows", fo.sequence_rows)
+    monkeypatch.setitem(fo.__dict__, "_orig_append_kv", fo.append_kv)
     for attr, fn in MUTANTS[name].items():
         monkeypatch.setattr(fo, attr, fn)
         if hasattr(oracle, attr):
