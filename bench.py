@@ -43,6 +43,8 @@ def parse_args():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--batch", type=int, default=0,
                     help="run the workload with this batch size instead of its own (smaller profiling captures)")
+    ap.add_argument("--append", action="store_true",
+                    help="fused append-KV + decode (fd_append_decode): each step writes the last token's k/v")
     ap.add_argument("--rows", type=int, default=1,
                     help="query rows per sequence (causal window through fd_decode_rows); 1 = fd_decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -306,8 +308,12 @@ def run_fdecode(args):
     if args.batch > 0:
         spec = dataclasses.replace(spec, B=args.batch, name=f"{spec.name}_batch{args.batch}")
     n_q = args.rows
+    if n_q > 1 and args.append:
+        raise SystemExit("--rows and --append are separate variants")
     if n_q > 1:
         spec = dataclasses.replace(spec, name=f"{spec.name}_rows{n_q}_causal")
+    if args.append:
+        spec = dataclasses.replace(spec, name=f"{spec.name}_append")
     case = make_case(spec, device)
     kv_bytes = case.kv_bytes()
     step_bytes = kv_bytes + spec.B * spec.Hq * n_q * spec.D * 4 * 2
@@ -324,6 +330,19 @@ def run_fdecode(args):
             fd.decode_rows(q_rows, case.k, case.v, causal=True, seq_lens=case.seq_lens,
                            max_seq_len=case.max_seq_len, block_table=case.block_table, scale=spec.scale,
                            n_splits=spec.n_splits, out=out, lse=lse, workspace=ws)
+    elif args.append:
+        # the sequences' last token is the one appended: lengths before the append are L_b - 1
+        lens_full = torch.tensor(case.lengths, dtype=torch.int32, device=device)
+        seq_before = (lens_full - 1).contiguous()
+        gen = torch.Generator(device=device).manual_seed(spec.seed + 29)
+        k_new = torch.randn((spec.B, spec.Hkv, spec.D), generator=gen, device=device).to(case.k.dtype)
+        v_new = torch.randn((spec.B, spec.Hkv, spec.D), generator=gen, device=device).to(case.k.dtype)
+        step_bytes += 2 * k_new.numel() * k_new.element_size()  # the new rows, read and stored
+
+        def step():
+            fd.append_decode(case.q, case.k, case.v, k_new, v_new, seq_lens=seq_before,
+                             max_seq_len=case.max_seq_len - 1, block_table=case.block_table, scale=spec.scale,
+                             n_splits=spec.n_splits, out=out, lse=lse, workspace=ws)
     else:
         def step():
             fd.decode(case.q, case.k, case.v, seq_lens=case.seq_lens, max_seq_len=case.max_seq_len,
@@ -372,7 +391,20 @@ def run_fdecode(args):
     lse_h = torch.empty(rows_shape, dtype=torch.float32, pin_memory=True)
     ws_h = fd.Workspace()
     e2e_api = "fd_decode_host"
-    if n_q > 1:
+    if args.append:
+        e2e_api = "pinned copies + fd_append_decode"
+        q_dev = torch.empty_like(case.q)
+        out_d, lse_d = torch.empty_like(out), torch.empty_like(lse)
+
+        def e2e_step():
+            q_dev.copy_(q_host, non_blocking=True)
+            fd.append_decode(q_dev, case.k, case.v, k_new, v_new, seq_lens=seq_before,
+                             max_seq_len=case.max_seq_len - 1, block_table=case.block_table, scale=spec.scale,
+                             n_splits=spec.n_splits, out=out_d, lse=lse_d, workspace=ws_h)
+            out_h.copy_(out_d, non_blocking=True)
+            lse_h.copy_(lse_d, non_blocking=True)
+            torch.cuda.current_stream(device).synchronize()
+    elif n_q > 1:
         e2e_api = "pinned copies + fd_decode_rows"
         q_dev = torch.empty_like(q_rows)
         lens_dev = None if lens_host is None else torch.empty_like(case.seq_lens)
@@ -405,7 +437,7 @@ def run_fdecode(args):
     te1 = time.perf_counter()
     e2e_s = max_over_ranks(te1 - te0, world, device)
     e2e_value = world * step_bytes * k_e2e / e2e_s / 1e9
-    h2d = q_host.numel() * 4 + (0 if lens_host is None else lens_host.numel() * 4)
+    h2d = q_host.numel() * 4 + (0 if lens_host is None or args.append else lens_host.numel() * 4)
     d2h = out_h.numel() * 4 + lse_h.numel() * 4
 
     if rank != 0:
@@ -415,7 +447,7 @@ def run_fdecode(args):
         return 0
     # ---- CPU baseline: the oracle on a bounded sample, host cores, rank 0 at N=1
     cpu = None
-    if world == 1 and not args.no_cpu_baseline and n_q == 1:
+    if world == 1 and not args.no_cpu_baseline and n_q == 1 and not args.append:
         v, note, el = OracleSampler(case).whole_groups(args.cpu_seconds)
         cpu = {"value": v, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle", "sample": note,
                "seconds": round(el, 2)}
@@ -432,7 +464,7 @@ def run_fdecode(args):
         "data": "synthetic",
         "config": {"workload": spec.name, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "D": spec.D,
                    "T": spec.T_cap, "kv_dtype": spec.kv_dtype, "q_dtype": "f32", "layout": spec.layout,
-                   "rows": n_q,
+                   "rows": n_q, "append": bool(args.append),
                    "kv_bytes_per_step": kv_bytes, "bytes_per_step": step_bytes,
                    "l2": f"inputs {kv_bytes / 1e6:.0f} MB > 129 MB L2; no flush",
                    "plan": "balanced" if spec.n_splits == 0 else f"n_splits={spec.n_splits}",

@@ -176,6 +176,30 @@ FD_API fd_status fd_decode_rows(const float* q, int32_t n_q, int32_t causal, con
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * Fused append-KV + decode (the "fused append-KV" path named in "FlashDecoding
+ * and split-KV", section "Walking through it"; the operation is this
+ * library's reading of it): for every sequence b the new token's key and
+ * value are written into the cache at position L_b and the decode then
+ * attends the L_b + 1 keys, in one launch.  The result equals writing the row
+ * first and calling fd_decode with lengths L_b + 1 (bit for bit).
+ *   k_new, v_new  [B, Hkv, D] device, in the cache dtype (kv->dtype), 16-byte
+ *                 aligned; their bits are stored unchanged.
+ *   seq_lens / max_seq_len  the lengths BEFORE the append (seq_lens is read,
+ *                 not updated: the caller advances its lengths).
+ *   kv            kv->k and kv->v are written (one row per (b, KV head)).
+ *                 Contiguous: capacity >= max_seq_len + 1.  Paged: the page
+ *                 holding position L_b must already be in the block table;
+ *                 an entry outside [0, num_pages) skips the cache write and
+ *                 is reported as FD_ERR_BAD_INDEX by fd_workspace_status (the
+ *                 output still includes the new token).
+ *   Other arguments as in fd_decode; the workspace is the same size.
+ */
+FD_API fd_status fd_append_decode(const float* q, const void* k_new, const void* v_new, const fd_kv_desc* kv,
+                                  float* out, float* lse, int32_t B, int32_t Hq, int32_t Hkv,
+                                  const int32_t* seq_lens, int32_t max_seq_len, int32_t D, float scale,
+                                  int32_t n_splits, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Split step only ("fd_split" of the walkthrough), with n_splits > 0 splits
  * per sequence of fd_split_size(max_seq_len, n_splits) tokens each.  Writes:
  *   o_part [B, Hq, n_splits, D]  unnormalised sum_t exp(s_t - m_s) v_t

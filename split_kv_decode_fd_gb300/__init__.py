@@ -14,6 +14,7 @@ from .fdecode import (  # noqa: F401
     decode,
     decode_host,
     decode_rows,
+    append_decode,
     decode_static,
     library_path,
     load_library,

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -287,15 +288,26 @@ fd_status fd_workspace_status(void* workspace, size_t workspace_bytes, void* str
 namespace {
 
 // fd_decode over Hq "virtual heads" = query heads x rows (n_q rows per head).
+// Variants of the decode: several query rows per head; the fused append.
+struct DecodeExtras {
+  int32_t n_q = 1, causal = 0;
+  const void* k_new = nullptr;  // non-null: append the new token before attending
+  const void* v_new = nullptr;
+};
+
 fd_status decode_impl(const float* q, const fd_kv_desc* kv, float* out, float* lse, int32_t B, int32_t Hq,
                       int32_t Hkv, const int32_t* seq_lens, int32_t max_seq_len, int32_t D, float scale,
-                      int32_t n_splits, void* workspace, size_t workspace_bytes, void* stream, int32_t n_q,
-                      int32_t causal) {
+                      int32_t n_splits, void* workspace, size_t workspace_bytes, void* stream,
+                      const DecodeExtras& x) {
   fd_status st = check_shape(B, Hq, Hkv, D);
   if (st != FD_OK) return st;
   if (!q || !out || !workspace || !aligned16(q) || !aligned16(out) || !aligned16(workspace))
     return FD_ERR_INVALID_ARG;
   if (n_splits < 0 || n_splits > 65535) return FD_ERR_INVALID_ARG;
+  const int32_t append = x.k_new ? 1 : 0;
+  if (append && (!x.v_new || !aligned16(x.k_new) || !aligned16(x.v_new) || max_seq_len < 0)) return FD_ERR_INVALID_ARG;
+  if (max_seq_len > INT32_MAX - append) return FD_ERR_UNSUPPORTED;
+  max_seq_len += append;  // from here on: lengths as the kernel sees them (the new token included)
   if ((st = check_kv(kv, B, Hkv, max_seq_len)) != FD_OK) return st;
   const Groups gr = make_groups(Hq, Hkv, group_cap(kv->dtype));
   const int64_t pairs = (int64_t)B * gr.hv;
@@ -309,8 +321,14 @@ fd_status decode_impl(const float* q, const fd_kv_desc* kv, float* out, float* l
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   SplitParams p = base_params(q, kv, B, Hq, Hkv, seq_lens, max_seq_len, scale);
-  p.n_q = n_q;
-  p.causal = causal;
+  p.n_q = x.n_q;
+  p.causal = x.causal;
+  p.append = append;
+  p.k_new = x.k_new;
+  p.v_new = x.v_new;
+  p.k_cache = const_cast<void*>(kv->k);
+  p.v_cache = const_cast<void*>(kv->v);
+  p.capacity = kv->capacity;
   p.out = out;
   p.lse = lse;
   p.o_part = reinterpret_cast<float*>(ws + w.o);
@@ -345,7 +363,19 @@ fd_status fd_decode(const float* q, const fd_kv_desc* kv, float* out, float* lse
                     int32_t Hkv, const int32_t* seq_lens, int32_t max_seq_len, int32_t D, float scale,
                     int32_t n_splits, void* workspace, size_t workspace_bytes, void* stream) {
   return decode_impl(q, kv, out, lse, B, Hq, Hkv, seq_lens, max_seq_len, D, scale, n_splits, workspace,
-                     workspace_bytes, stream, 1, 0);
+                     workspace_bytes, stream, DecodeExtras{});
+}
+
+fd_status fd_append_decode(const float* q, const void* k_new, const void* v_new, const fd_kv_desc* kv, float* out,
+                           float* lse, int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_lens,
+                           int32_t max_seq_len, int32_t D, float scale, int32_t n_splits, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (!k_new || !v_new) return FD_ERR_INVALID_ARG;
+  DecodeExtras x;
+  x.k_new = k_new;
+  x.v_new = v_new;
+  return decode_impl(q, kv, out, lse, B, Hq, Hkv, seq_lens, max_seq_len, D, scale, n_splits, workspace,
+                     workspace_bytes, stream, x);
 }
 
 fd_status fd_decode_rows(const float* q, int32_t n_q, int32_t causal, const fd_kv_desc* kv, float* out,
@@ -354,8 +384,11 @@ fd_status fd_decode_rows(const float* q, int32_t n_q, int32_t causal, const fd_k
                          size_t workspace_bytes, void* stream) {
   if (n_q < 1 || n_q > 64 || (causal != 0 && causal != 1)) return FD_ERR_INVALID_ARG;
   if (Hq < 1 || (int64_t)Hq * n_q > ((int64_t)1 << 24)) return FD_ERR_INVALID_ARG;
+  DecodeExtras x;
+  x.n_q = n_q;
+  x.causal = causal;
   return decode_impl(q, kv, out, lse, B, Hq * n_q, Hkv, seq_lens, max_seq_len, D, scale, n_splits, workspace,
-                     workspace_bytes, stream, n_q, causal);
+                     workspace_bytes, stream, x);
 }
 
 fd_status fd_split_partial(const float* q, const fd_kv_desc* kv, int32_t B, int32_t Hq, int32_t Hkv,

@@ -66,6 +66,15 @@ struct SplitParams {
   float qk_scale;          // scale * log2(e)
   int32_t n_q;             // query rows per (b, head): virtual head h' = head * n_q + row
   int32_t causal;          // rows see keys t < L_b - (n_q - 1 - row) (else all L_b keys)
+  // Fused append: the new token's k/v ([B, Hkv, D], cache dtype) join every
+  // sequence at position L_b (seq_lens are the lengths before the append; the
+  // plan sees L_b + 1) and are written into the cache at that position.
+  int32_t append;
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;           // the cache's K and V base pointers (pool when paged)
+  void* v_cache;
+  int64_t capacity;        // contiguous: rows per (b, KV head)
 };
 
 // Keys seen by the heads of one piece: head0 + j for j < nh; virtual head
@@ -330,7 +339,7 @@ struct PieceIter {
     const int32_t pair = blockIdx.x, s = blockIdx.y;
     pc.b = pair / p.hv;
     pc.vkv = pair % p.hv;
-    const int32_t L = p.seq_lens ? clamp_len(__ldg(p.seq_lens + pc.b), p.max_len) : p.max_len;
+    const int32_t L = p.seq_lens ? clamp_len(__ldg(p.seq_lens + pc.b) + p.append, p.max_len) : p.max_len;
     const int64_t lo = (int64_t)s * p.split_tokens;
     const int64_t hi = lo + p.split_tokens < L ? lo + p.split_tokens : L;
     pc.tok_begin = (int32_t)(lo < L ? lo : L);
@@ -674,6 +683,51 @@ struct CoreEngine {
   }
 };
 
+// Fused append: put the new token's K and V row (position L = len - 1 of the
+// sequence, row r of the stage) into the landed stage, in the 128-byte-swizzle
+// layout the TMA boxes use (16-byte chunk c of row r sits in column block c/8
+// at chunk (c % 8) ^ (r % 8)), and, when `to_cache`, into the cache itself.
+// Only warp r / 32 reads row r, so the warp's own fence and __syncwarp order
+// these stores before its reads and before the stage's next TMA write.
+template <class C>
+__device__ __forceinline__ void append_row(const SplitParams& p, int32_t b, int32_t kvh, int32_t L, int32_t r,
+                                           uint32_t kst, uint32_t vst, int lane, bool to_cache) {
+  constexpr int kChunks = C::kRowBytes / 16;
+  const size_t src = ((size_t)b * p.Hkv + kvh) * C::kRowBytes;
+  const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.k_new) + src);
+  const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.v_new) + src);
+  size_t dst = 0;
+  if (to_cache) {
+    if (p.paged) {
+      const int32_t page = __ldg(p.block_table + (size_t)b * p.max_pages + L / p.page_size);
+      if (page < 0 || page >= p.num_pages) {
+        if (lane == 0) raise_error(p.err, kErrBadIndex);
+        to_cache = false;
+      } else {
+        dst = (((size_t)page * p.Hkv + kvh) * p.page_size + L % p.page_size) * C::kRowBytes;
+      }
+    } else {
+      dst = (((size_t)b * p.Hkv + kvh) * p.capacity + L) * C::kRowBytes;
+    }
+  }
+  for (int c = lane; c < kChunks; c += 32) {
+    const uint4 kx = __ldg(ks + c), vx = __ldg(vs + c);
+    const uint32_t so = (uint32_t)(c >> 3) * C::kBT * 128 + (uint32_t)r * 128 + ((uint32_t)((c & 7) ^ (r & 7)) << 4);
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(kst + so), "r"(kx.x), "r"(kx.y), "r"(kx.z),
+                 "r"(kx.w)
+                 : "memory");
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(vst + so), "r"(vx.x), "r"(vx.y), "r"(vx.z),
+                 "r"(vx.w)
+                 : "memory");
+    if (to_cache) {
+      reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.k_cache) + dst)[c] = kx;
+      reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.v_cache) + dst)[c] = vx;
+    }
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+}
+
 template <class C, class E>
 __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTiles& tl, int64_t total,
                                                uint8_t* smem, volatile int* abort_flag) {
@@ -747,6 +801,10 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
         nv = nv < 0 ? 0 : (nv > 32 ? 32 : nv);
         if (nv > 0) {
           const uint32_t kst = sbase + stage * C::kStageBytes;
+          // the new token is the last key of the sequence: this piece's last tile, this warp's last row
+          if (p.append && pc.tok_end == pc.len && nvalid == 32 * warp + nv && t0 + nvalid == pc.len)
+            append_row<C>(p, pc.b, kv_head_of_vkv(gr, pc.vkv), pc.len - 1, nvalid - 1, kst, kst + C::kTileBytes,
+                          lane, pc.vkv % gr.nsub == 0);
           eng.tile(kst, kst + C::kTileBytes, nv, qaddr, p.qk_scale, t0);
         }
         if (lane == 0) mbar_arrive(empty + stage);
@@ -916,7 +974,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   tl.uniform = 1;
   if (p.n_splits == 0 && p.seq_lens != nullptr) {
     tl.uniform = 0;
-    for (int b = tid; b < p.B; b += C::kThreads) lens[b] = clamp_len(__ldg(p.seq_lens + b), p.max_len);
+    for (int b = tid; b < p.B; b += C::kThreads) lens[b] = clamp_len(__ldg(p.seq_lens + b) + p.append, p.max_len);
     __syncthreads();
     if (warp == 0) {
       const int lane = tid & 31;

@@ -17,7 +17,7 @@ import numpy as np
 
 __all__ = [
     "FdError", "KvDesc", "library_path", "load_library", "workspace_bytes", "split_size", "plan_pieces",
-    "Workspace", "decode", "decode_rows", "decode_host", "decode_static", "split_partial", "combine", "workspace_status",
+    "Workspace", "decode", "decode_rows", "append_decode", "decode_host", "decode_static", "split_partial", "combine", "workspace_status",
 ]
 
 FD_OK, FD_ERR_INVALID_ARG, FD_ERR_UNSUPPORTED, FD_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3
@@ -87,6 +87,8 @@ def load_library(path: Optional[str] = None):
                                                 c_i32, vp]),
             "fd_decode_rows": (ctypes.c_int, [vp, c_i32, c_i32, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32,
                                               c_i32, f32, c_i32, vp, c_sz, vp]),
+            "fd_append_decode": (ctypes.c_int, [vp, vp, vp, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32, c_i32, f32,
+                                                c_i32, vp, c_sz, vp]),
             "fd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "fd_version": (c_i32, []),
         }
@@ -281,6 +283,47 @@ def decode_rows(q, k, v, *, causal=True, seq_lens=None, max_seq_len=None, block_
                                float(scale), int(n_splits), buf.data_ptr(), buf.numel(),
                                _stream_handle(q.device, stream))
     _check(st, "fd_decode_rows")
+    return out, lse
+
+
+def append_decode(q, k, v, k_new, v_new, *, seq_lens=None, max_seq_len=None, block_table=None, scale=None,
+                  n_splits=FD_SPLITS_AUTO, out=None, lse=None, return_lse=True,
+                  workspace: Optional[Workspace] = None, stream=None):
+    """``fd_append_decode``: write ``k_new``/``v_new`` (``[B, Hkv, D]``, cache dtype) at
+    position ``L_b`` of every sequence, then decode over ``L_b + 1`` keys.
+
+    ``seq_lens``/``max_seq_len`` are the lengths before the append (default
+    ``max_seq_len``: the cache capacity minus one).  ``k`` and ``v`` are written.
+    Returns ``(out, lse)``.
+    """
+    torch = _torch()
+    _need_cuda(q, "q", torch.float32)
+    kv = _kv_desc(k, v, block_table)
+    _need_cuda(k_new, "k_new", k.dtype)
+    _need_cuda(v_new, "v_new", k.dtype)
+    B, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D):
+        raise ValueError("k_new and v_new must be [B, Hkv, D]")
+    if max_seq_len is None:
+        cap = k.shape[2] if block_table is None else block_table.shape[1] * k.shape[2]
+        max_seq_len = cap - 1
+    if seq_lens is not None:
+        _need_cuda(seq_lens, "seq_lens", torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    ws = workspace or _default_workspace(q.device)
+    buf = ws.get(workspace_bytes(B, Hq, Hkv, D, n_splits), q.device)
+    st = _lib().fd_append_decode(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), ctypes.byref(kv), out.data_ptr(),
+                                 lse.data_ptr() if lse is not None else None, B, Hq, Hkv,
+                                 seq_lens.data_ptr() if seq_lens is not None else None, int(max_seq_len), D,
+                                 float(scale), int(n_splits), buf.data_ptr(), buf.numel(),
+                                 _stream_handle(q.device, stream))
+    _check(st, "fd_append_decode")
     return out, lse
 
 

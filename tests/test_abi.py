@@ -237,3 +237,19 @@ def test_decode_rows_rejects_bad_window(lib, n_q, causal, expected):
     st = lib.fd_decode_rows(FAKE, n_q, causal, ctypes.byref(kv), FAKE, None, 1, 4, 4, None, 1024, 128, 0.1, 4,
                             FAKE, 1024, None)
     assert st == expected
+
+
+@pytest.mark.parametrize("case,expected", [
+    (dict(k_new=0), fdb.FD_ERR_INVALID_ARG),
+    (dict(v_new=0), fdb.FD_ERR_INVALID_ARG),
+    (dict(k_new=FAKE + 8), fdb.FD_ERR_INVALID_ARG),
+    (dict(max_len=1024), fdb.FD_ERR_INVALID_ARG),  # the new token needs row 1024 of a 1024-row cache
+    (dict(max_len=-1), fdb.FD_ERR_INVALID_ARG),
+    (dict(max_len=1023, ws_bytes=1024), fdb.FD_ERR_WORKSPACE_TOO_SMALL),  # valid; the workspace is too small
+])
+def test_append_decode_rejects_bad_arguments(lib, case, expected):
+    kv = _kv()
+    st = lib.fd_append_decode(FAKE, case.get("k_new", FAKE + 8192), case.get("v_new", FAKE + 12288),
+                              ctypes.byref(kv), FAKE, None, 1, 4, 4, None, case.get("max_len", 1023), 128, 0.1, 4,
+                              FAKE, case.get("ws_bytes", 1 << 30), None)
+    assert st == expected
