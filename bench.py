@@ -47,6 +47,8 @@ def parse_args():
                     help="fused append-KV + decode (fd_append_decode): each step writes the last token's k/v")
     ap.add_argument("--rows", type=int, default=1,
                     help="query rows per sequence (causal window through fd_decode_rows); 1 = fd_decode")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time K plain stream launches instead of one CUDA graph of K launches")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -355,9 +357,30 @@ def run_fdecode(args):
     if fd.workspace_status(ws) != 0:
         raise SystemExit("kernel reported an error during warm-up")
 
-    # ---- timed region: K steps, per-launch events, clocks sampled meanwhile
+    # ---- per-launch spread (diagnostic, outside the timed region): events around single launches
+    n_ev = min(200, max(20, args.steps))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    launch_us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+
+    # ---- timed region: K steps back to back (one CUDA graph of K launches unless --no-graph),
+    # CUDA events on the launching stream around the whole region, clocks sampled meanwhile
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(K):
+                step()
+        torch.cuda.synchronize()
+        graph.replay()  # one untimed replay: the graph's first launch uploads it
+        torch.cuda.synchronize()
+        if fd.workspace_status(ws) != 0:
+            raise SystemExit("kernel reported an error in the captured steps")
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(device.index or 0)
     sampler.start()
@@ -366,21 +389,22 @@ def run_fdecode(args):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     start.record(stream)
-    for i in range(K):
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for _ in range(K):
+            step()
     end.record(stream)
     torch.cuda.synchronize()
     t1 = time.perf_counter()
     barrier(world)
     clocks = sampler.stop(t0, t1)
     total_ms = start.elapsed_time(end)
-    launch_us = [a.elapsed_time(b) * 1e3 for a, b in ev]
     total_ms = max_over_ranks(total_ms, world, device)
     ms_per_step = total_ms / K
     value = world * step_bytes * K / (total_ms * 1e-3) / 1e9
-    mean_launch_us = statistics.mean(launch_us)
+    # one launch per step, back to back: the average launch duration is the region / K
+    mean_launch_us = ms_per_step * 1e3
     achieved = step_bytes / (mean_launch_us * 1e-6) / 1e9
     peak, peak_src = measured_peak()
 
@@ -470,7 +494,9 @@ def run_fdecode(args):
                    "plan": "balanced" if spec.n_splits == 0 else f"n_splits={spec.n_splits}",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "kernel": f"fd_split_kernel<D={spec.D},{spec.kv_dtype},G={gpad}> (fused LSE merge)",
-                   "launch_us_p10_p50_p90": [round(x, 2) for x in statistics.quantiles(launch_us, n=10)[0::4]]},
+                   "launch": "one CUDA graph of K fd_decode-family calls" if graph is not None else "K stream launches",
+                   "single_launch_event_us_p10_p50_p90": [round(x, 2) for x in
+                                                          statistics.quantiles(launch_us, n=10)[0::4]]},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(spec.name),
                      "peak_source": peak_src, "kernel": "fd_split_kernel", "launches_per_step": 1,

@@ -156,6 +156,26 @@ fd_status make_maps(const fd_kv_desc* kv, int B, int Hkv, int D, CUtensorMap* tk
     box[1] = 16;
     box[2] = 1;
   }
+  // Encoding costs a driver call per map; decode steps usually repeat the same
+  // cache, so the last few (K, V) pairs are kept per host thread, keyed by
+  // every input of the encoding (a map holds nothing else).
+  struct MapEntry {
+    const void *k, *v;
+    CUtensorMapDataType dt;
+    cuuint64_t dims[3], strides[2];
+    CUtensorMap tk, tv;
+    bool valid;
+  };
+  thread_local MapEntry cache[4];
+  thread_local int next_slot = 0;
+  for (const MapEntry& e : cache) {
+    if (e.valid && e.k == kv->k && e.v == kv->v && e.dt == dt && e.dims[0] == dims[0] && e.dims[1] == dims[1] &&
+        e.dims[2] == dims[2] && e.strides[0] == strides[0] && e.strides[1] == strides[1]) {
+      *tk = e.tk;
+      *tv = e.tv;
+      return FD_OK;
+    }
+  }
   const void* ptrs[2] = {kv->k, kv->v};
   CUtensorMap* maps[2] = {tk, tv};
   for (int i = 0; i < 2; ++i) {
@@ -164,6 +184,16 @@ fd_status make_maps(const fd_kv_desc* kv, int B, int Hkv, int D, CUtensorMap* tk
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return FD_ERR_INVALID_ARG;
   }
+  MapEntry& e = cache[next_slot];
+  next_slot = (next_slot + 1) % 4;
+  e.k = kv->k;
+  e.v = kv->v;
+  e.dt = dt;
+  for (int i = 0; i < 3; ++i) e.dims[i] = dims[i];
+  for (int i = 0; i < 2; ++i) e.strides[i] = strides[i];
+  e.tk = *tk;
+  e.tv = *tv;
+  e.valid = true;
   return FD_OK;
 }
 
