@@ -684,49 +684,65 @@ struct CoreEngine {
 };
 
 // Fused append: put the new token's K and V row (position L = len - 1 of the
-// sequence, row r of the stage) into the landed stage, in the 128-byte-swizzle
-// layout the TMA boxes use (16-byte chunk c of row r sits in column block c/8
-// at chunk (c % 8) ^ (r % 8)), and, when `to_cache`, into the cache itself.
-// Only warp r / 32 reads row r, so the warp's own fence and __syncwarp order
-// these stores before its reads and before the stage's next TMA write.
+// sequence, row r of its last stage) into the landed stage, in the
+// 128-byte-swizzle layout the TMA boxes use (16-byte chunk c of row r sits in
+// column block c/8 at chunk (c % 8) ^ (r % 8)), and, when `to_cache`, into the
+// cache itself.  The owning warp loads its chunks (lane c holds chunk c) and
+// looks up the cache position when the piece starts, so those loads overlap
+// the piece's streaming.  Only warp r / 32 reads row r, so the warp's own
+// fence and __syncwarp order the stores before its reads and before the
+// stage's next TMA write.
 template <class C>
-__device__ __forceinline__ void append_row(const SplitParams& p, int32_t b, int32_t kvh, int32_t L, int32_t r,
-                                           uint32_t kst, uint32_t vst, int lane, bool to_cache) {
-  constexpr int kChunks = C::kRowBytes / 16;
-  const size_t src = ((size_t)b * p.Hkv + kvh) * C::kRowBytes;
-  const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.k_new) + src);
-  const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.v_new) + src);
-  size_t dst = 0;
-  if (to_cache) {
-    if (p.paged) {
-      const int32_t page = __ldg(p.block_table + (size_t)b * p.max_pages + L / p.page_size);
-      if (page < 0 || page >= p.num_pages) {
-        if (lane == 0) raise_error(p.err, kErrBadIndex);
-        to_cache = false;
-      } else {
-        dst = (((size_t)page * p.Hkv + kvh) * p.page_size + L % p.page_size) * C::kRowBytes;
-      }
-    } else {
-      dst = (((size_t)b * p.Hkv + kvh) * p.capacity + L) * C::kRowBytes;
+struct AppendRow {
+  static constexpr int kChunks = C::kRowBytes / 16;
+  static_assert(kChunks <= 32, "one 16-byte chunk per lane");
+  uint4 kx, vx;
+  size_t dst;
+  bool to_cache;
+
+  __device__ __forceinline__ void prefetch(const SplitParams& p, int32_t b, int32_t kvh, int32_t L, int lane,
+                                           bool cache_write) {
+    const size_t src = ((size_t)b * p.Hkv + kvh) * C::kRowBytes;
+    if (lane < kChunks) {
+      kx = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.k_new) + src) + lane);
+      vx = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.v_new) + src) + lane);
     }
-  }
-  for (int c = lane; c < kChunks; c += 32) {
-    const uint4 kx = __ldg(ks + c), vx = __ldg(vs + c);
-    const uint32_t so = (uint32_t)(c >> 3) * C::kBT * 128 + (uint32_t)r * 128 + ((uint32_t)((c & 7) ^ (r & 7)) << 4);
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(kst + so), "r"(kx.x), "r"(kx.y), "r"(kx.z),
-                 "r"(kx.w)
-                 : "memory");
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(vst + so), "r"(vx.x), "r"(vx.y), "r"(vx.z),
-                 "r"(vx.w)
-                 : "memory");
+    to_cache = cache_write;
+    dst = 0;
     if (to_cache) {
-      reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.k_cache) + dst)[c] = kx;
-      reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.v_cache) + dst)[c] = vx;
+      if (p.paged) {
+        const int32_t page = __ldg(p.block_table + (size_t)b * p.max_pages + L / p.page_size);
+        if (page < 0 || page >= p.num_pages) {
+          if (lane == 0) raise_error(p.err, kErrBadIndex);
+          to_cache = false;
+        } else {
+          dst = (((size_t)page * p.Hkv + kvh) * p.page_size + L % p.page_size) * C::kRowBytes;
+        }
+      } else {
+        dst = (((size_t)b * p.Hkv + kvh) * p.capacity + L) * C::kRowBytes;
+      }
     }
   }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  __syncwarp();
-}
+
+  __device__ __forceinline__ void place(const SplitParams& p, uint32_t kst, uint32_t vst, int32_t r, int lane) {
+    if (lane < kChunks) {
+      const int c = lane;
+      const uint32_t so = (uint32_t)(c >> 3) * C::kBT * 128 + (uint32_t)r * 128 + ((uint32_t)((c & 7) ^ (r & 7)) << 4);
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(kst + so), "r"(kx.x), "r"(kx.y), "r"(kx.z),
+                   "r"(kx.w)
+                   : "memory");
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(vst + so), "r"(vx.x), "r"(vx.y), "r"(vx.z),
+                   "r"(vx.w)
+                   : "memory");
+      if (to_cache) {
+        reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.k_cache) + dst)[c] = kx;
+        reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.v_cache) + dst)[c] = vx;
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+  }
+};
 
 template <class C, class E>
 __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTiles& tl, int64_t total,
@@ -776,6 +792,13 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
     const bool nonempty = pc.tok_end > pc.tok_begin;
     eng.reset();
     const uint32_t qslot = qi % C::kQBufs;
+    // Fused append: the warp owning the new token's row prefetches it now.
+    const bool app = p.append && nonempty && pc.tok_end == pc.len;
+    const int32_t app_t0 = pc.tok_begin + (pc.tok_end - 1 - pc.tok_begin) / C::kBT * C::kBT;  // last tile
+    const int32_t app_r = pc.tok_end - 1 - app_t0;                                          // its row
+    AppendRow<C> arow;
+    if (app && warp == (app_r >> 5))
+      arow.prefetch(p, pc.b, kv_head_of_vkv(gr, pc.vkv), pc.len - 1, lane, pc.vkv % gr.nsub == 0);
     if (nonempty && ok) {
       if (!mbar_wait(qfull + qslot, (qi / C::kQBufs) & 1)) {
         ok = false;
@@ -801,10 +824,8 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
         nv = nv < 0 ? 0 : (nv > 32 ? 32 : nv);
         if (nv > 0) {
           const uint32_t kst = sbase + stage * C::kStageBytes;
-          // the new token is the last key of the sequence: this piece's last tile, this warp's last row
-          if (p.append && pc.tok_end == pc.len && nvalid == 32 * warp + nv && t0 + nvalid == pc.len)
-            append_row<C>(p, pc.b, kv_head_of_vkv(gr, pc.vkv), pc.len - 1, nvalid - 1, kst, kst + C::kTileBytes,
-                          lane, pc.vkv % gr.nsub == 0);
+          // the new token is the last key of the sequence: this piece's last tile, row app_r
+          if (app && t0 == app_t0 && warp == (app_r >> 5)) arow.place(p, kst, kst + C::kTileBytes, app_r, lane);
           eng.tile(kst, kst + C::kTileBytes, nv, qaddr, p.qk_scale, t0);
         }
         if (lane == 0) mbar_arrive(empty + stage);
