@@ -49,6 +49,8 @@ def parse_args():
                     help="query rows per sequence (causal window through fd_decode_rows); 1 = fd_decode")
     ap.add_argument("--no-graph", action="store_true",
                     help="time K plain stream launches instead of one CUDA graph of K launches")
+    ap.add_argument("--prefill", type=int, default=0, metavar="N",
+                    help="time fd_prefill on an N-token causal prompt (B=1, Hq=32, Hkv=8, D=128): TFLOP/s")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -75,6 +77,19 @@ def measured_peak():
         return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+def measured_tensor_peak():
+    """Dense bf16 tensor peak: MEASURED_PEAKS.json (burst figure: a kernel timed alone), else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        for key in ("bf16_tflops", "bf16_tflops_burst"):
+            if key in d and float(d[key]) > 0:
+                return float(d[key]), f"measured (MEASURED_PEAKS.json {key}, cuBLAS bf16 GEMM)"
+    except (OSError, ValueError, TypeError):
+        pass
+    return 1900.0, "fallback (1.9 PFLOP/s bf16 burst, one earlier GB300 measurement)"
 
 
 def recorded_traffic(workload_name: str):
@@ -516,10 +531,117 @@ def run_fdecode(args):
     return 0
 
 
+def run_prefill(args):
+    """fd_prefill on an N-token causal prompt whose keys fill the cache: a tensor-bound step."""
+    world, rank, local = dist_env()
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (libfdecode has no CPU path)")
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    import split_kv_decode_fd_gb300 as fd
+    from workloads import make_case, small_spec
+    fd.load_library()
+    N = args.prefill
+    spec = small_spec(f"prefill_causal_B1_Hq32_Hkv8_N{N}", 1, 32, 8, 128, N, seed=1003)
+    case = make_case(spec, device)
+    gen = torch.Generator(device=device).manual_seed(spec.seed + 31)
+    q = torch.randn((1, 32, N, 128), generator=gen, device=device)
+    out = torch.empty_like(q)
+    lse = torch.empty((1, 32, N), device=device)
+    ws = fd.Workspace()
+
+    def step():
+        fd.prefill(q, case.k, case.v, causal=True, max_seq_len=N, scale=spec.scale, out=out, lse=lse, workspace=ws)
+
+    # useful flops: q.k and p.v over each row's causal keys (row i sees i + 1 keys), 2 per multiply-add
+    flops = 4.0 * 128 * 32 * (N * (N + 1) / 2)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if fd.workspace_status(ws) != 0:
+        raise SystemExit("kernel reported an error during warm-up")
+    K = args.steps
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(K):
+            step()
+    graph.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device.index or 0)
+    sampler.start()
+    time.sleep(0.2)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    start.record(stream)
+    graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    barrier(world)
+    clocks = sampler.stop(t0, t1)
+    total_ms = max_over_ranks(start.elapsed_time(end), world, device)
+    ms_per_step = total_ms / K
+    tflops = flops / (ms_per_step * 1e-3) / 1e12
+    peak, peak_src = measured_tensor_peak()
+    # end to end: host q in, host out + lse back, copies around fd_prefill
+    q_host = q.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=torch.float32, pin_memory=True)
+    lse_h = torch.empty(lse.shape, dtype=torch.float32, pin_memory=True)
+    q_dev = torch.empty_like(q)
+
+    def e2e_step():
+        q_dev.copy_(q_host, non_blocking=True)
+        fd.prefill(q_dev, case.k, case.v, causal=True, max_seq_len=N, scale=spec.scale, out=out, lse=lse,
+                   workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    k_e2e = max(5, min(K, 50))
+    te0 = time.perf_counter()
+    for _ in range(k_e2e):
+        e2e_step()
+    e2e_s = max_over_ranks(time.perf_counter() - te0, world, device)
+    if rank != 0:
+        return 0
+    line = {
+        "metric": "prefill attention TFLOP/s (useful causal flops)", "value": world * tflops, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16x2 (hi+lo) -> f32",
+        "data": "synthetic",
+        "config": {"workload": spec.name, "B": 1, "Hq": 32, "Hkv": 8, "D": 128, "n_q": N, "keys": N,
+                   "causal": True, "kv_dtype": "bf16", "q_dtype": "f32", "flops_per_step": flops,
+                   "launch": "one CUDA graph of K fd_prefill calls",
+                   "kernel": "fd_prefill_kernel (tcgen05.mma M=128; q and p as bf16 hi+lo: 2 MMAs per product)"},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                     "traffic": None, "peak_source": peak_src, "kernel": "fd_prefill_kernel",
+                     "launches_per_step": 1, "mean_launch_us": ms_per_step * 1e3},
+        "e2e": {"value": world * flops * k_e2e / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": q_host.numel() * 4, "d2h_bytes_per_step": (out_h.numel() + lse_h.numel()) * 4,
+                "steps": k_e2e, "api": "pinned copies + fd_prefill"},
+        "gpu_launches": K, "clocks": clocks, "cpu_baseline": None, "kernel_status": fd.workspace_status(ws),
+        "source_sha": source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.prefill:
+        return run_prefill(args)
     return run_fdecode(args)
 
 

@@ -200,6 +200,47 @@ FD_API fd_status fd_append_decode(const float* q, const void* k_new, const void*
                                   int32_t n_splits, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Attention for many query rows per sequence (prefill, or a long window of new
+ * tokens): the same operation as fd_decode_rows -- q [B, Hq, n_q, D], the rows
+ * are the last n_q tokens of each sequence, causal or not -- computed with
+ * query tiles of 128 rows on the tensor cores (tcgen05.mma, TMEM
+ * accumulators) instead of rows-as-heads.  "FlashDecoding and split-KV",
+ * section "Walking through it": prefill has many query rows and wants
+ * FlashAttention's tiling along them; decode has one.
+ *   Supports D = 128 with a bf16 cache (contiguous or paged); any n_q >= 1.
+ *   workspace: at least 256 bytes, zero-filled once (its first word is the
+ *   kernels' error word, read by fd_workspace_status).  out, lse as in
+ *   fd_decode_rows.  One launch, asynchronous on `stream`.
+ */
+FD_API fd_status fd_prefill(const float* q, int32_t n_q, int32_t causal, const fd_kv_desc* kv, float* out,
+                            float* lse, int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_lens,
+                            int32_t max_seq_len, int32_t D, float scale, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * Phase dispatch ("FlashDecoding and split-KV", "Walking through it": serving
+ * engines pick a kernel per phase and should log which one ran).  fd_attend
+ * picks the backend for n_q query rows per sequence and reports it:
+ *   FD_BACKEND_DECODE       n_q == 1                      -> fd_decode
+ *   FD_BACKEND_DECODE_ROWS  n_q * (Hq / Hkv) <= 16, or no prefill kernel for
+ *                           this D / dtype and n_q <= 64  -> fd_decode_rows
+ *   FD_BACKEND_PREFILL      otherwise (D = 128, bf16)     -> fd_prefill
+ * fd_attend_backend returns the choice without running anything (-1: no
+ * backend); fd_backend_name names it.  The workspace must fit the chosen
+ * backend: fd_workspace_bytes(B, Hq * n_q, Hkv, D, n_splits, 0) for the decode
+ * backends, 256 bytes for prefill.  *backend (may be NULL) receives the choice.
+ */
+#define FD_BACKEND_DECODE 0
+#define FD_BACKEND_DECODE_ROWS 1
+#define FD_BACKEND_PREFILL 2
+FD_API int32_t fd_attend_backend(int32_t n_q, int32_t Hq, int32_t Hkv, int32_t D, int32_t kv_dtype);
+FD_API const char* fd_backend_name(int32_t backend);
+FD_API fd_status fd_attend(const float* q, int32_t n_q, int32_t causal, const fd_kv_desc* kv, float* out,
+                           float* lse, int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_lens,
+                           int32_t max_seq_len, int32_t D, float scale, int32_t n_splits, void* workspace,
+                           size_t workspace_bytes, void* stream, int32_t* backend);
+
+/*
  * Split step only ("fd_split" of the walkthrough), with n_splits > 0 splits
  * per sequence of fd_split_size(max_seq_len, n_splits) tokens each.  Writes:
  *   o_part [B, Hq, n_splits, D]  unnormalised sum_t exp(s_t - m_s) v_t

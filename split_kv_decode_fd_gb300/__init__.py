@@ -15,6 +15,9 @@ from .fdecode import (  # noqa: F401
     decode_host,
     decode_rows,
     append_decode,
+    prefill,
+    attend,
+    attend_backend,
     decode_static,
     library_path,
     load_library,

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfdecode.so")
-SOURCES = ["fd_api.cu", "fd_combine.cu", "fd_split_bf16.cu", "fd_split_f32.cu"]
+SOURCES = ["fd_api.cu", "fd_combine.cu", "fd_split_bf16.cu", "fd_split_f32.cu", "fd_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

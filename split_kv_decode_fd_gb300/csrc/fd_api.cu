@@ -11,6 +11,7 @@
 
 #include "../../include/fdecode.h"
 #include "fd_internal.h"
+#include "fd_prefill.h"
 #include "fd_split.cuh"
 
 using namespace fdk;
@@ -419,6 +420,81 @@ fd_status fd_decode_rows(const float* q, int32_t n_q, int32_t causal, const fd_k
   x.causal = causal;
   return decode_impl(q, kv, out, lse, B, Hq * n_q, Hkv, seq_lens, max_seq_len, D, scale, n_splits, workspace,
                      workspace_bytes, stream, x);
+}
+
+fd_status fd_prefill(const float* q, int32_t n_q, int32_t causal, const fd_kv_desc* kv, float* out, float* lse,
+                     int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_lens, int32_t max_seq_len, int32_t D,
+                     float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  fd_status st = check_shape(B, Hq, Hkv, D);
+  if (st != FD_OK) return st;
+  if (!q || !out || !workspace || !aligned16(q) || !aligned16(out) || !aligned16(workspace))
+    return FD_ERR_INVALID_ARG;
+  if (n_q < 1 || (causal != 0 && causal != 1)) return FD_ERR_INVALID_ARG;
+  if (workspace_bytes < kHeaderBytes) return FD_ERR_WORKSPACE_TOO_SMALL;
+  if ((st = check_kv(kv, B, Hkv, max_seq_len)) != FD_OK) return st;
+  if (D != 128 || kv->dtype != FD_BF16) return FD_ERR_UNSUPPORTED;
+  if (B > 65535 || Hq > 65535 || (int64_t)B * Hq * n_q * D > ((int64_t)1 << 40)) return FD_ERR_UNSUPPORTED;
+  CUtensorMap tk, tv;
+  if ((st = make_maps(kv, B, Hkv, D, &tk, &tv)) != FD_OK) return st;
+  PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.out = out;
+  p.lse = lse;
+  p.seq_lens = seq_lens;
+  p.block_table = kv->block_table;
+  p.err = reinterpret_cast<unsigned*>(workspace);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.g = Hq / Hkv;
+  p.n_q = n_q;
+  p.max_len = max_seq_len;
+  p.causal = causal;
+  p.paged = kv->layout == FD_KV_PAGED;
+  p.page_size = kv->page_size;
+  p.max_pages = kv->max_pages_per_seq;
+  p.num_pages = kv->num_pages;
+  p.qk_scale = (float)((double)scale * 1.4426950408889634);
+  return launch_prefill(tk, tv, p, (cudaStream_t)stream) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+int32_t fd_attend_backend(int32_t n_q, int32_t Hq, int32_t Hkv, int32_t D, int32_t kv_dtype) {
+  if (n_q < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return -1;
+  if (n_q == 1) return FD_BACKEND_DECODE;
+  const bool prefill_ok = D == 128 && kv_dtype == FD_BF16;
+  if ((int64_t)n_q * (Hq / Hkv) <= kMaxGroupBf16 || (!prefill_ok && n_q <= 64)) return FD_BACKEND_DECODE_ROWS;
+  return prefill_ok ? FD_BACKEND_PREFILL : -1;
+}
+
+const char* fd_backend_name(int32_t backend) {
+  switch (backend) {
+    case FD_BACKEND_DECODE: return "decode (fd_split_kernel, one query row)";
+    case FD_BACKEND_DECODE_ROWS: return "decode_rows (fd_split_kernel, rows as virtual heads)";
+    case FD_BACKEND_PREFILL: return "prefill (fd_prefill_kernel, tcgen05 query tiles)";
+    default: return "none";
+  }
+}
+
+fd_status fd_attend(const float* q, int32_t n_q, int32_t causal, const fd_kv_desc* kv, float* out, float* lse,
+                    int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_lens, int32_t max_seq_len, int32_t D,
+                    float scale, int32_t n_splits, void* workspace, size_t workspace_bytes, void* stream,
+                    int32_t* backend) {
+  const int32_t be = fd_attend_backend(n_q, Hq, Hkv, D, kv ? kv->dtype : -1);
+  if (backend) *backend = be;
+  switch (be) {
+    case FD_BACKEND_DECODE:
+      return fd_decode(q, kv, out, lse, B, Hq, Hkv, seq_lens, max_seq_len, D, scale, n_splits, workspace,
+                       workspace_bytes, stream);
+    case FD_BACKEND_DECODE_ROWS:
+      return fd_decode_rows(q, n_q, causal, kv, out, lse, B, Hq, Hkv, seq_lens, max_seq_len, D, scale, n_splits,
+                            workspace, workspace_bytes, stream);
+    case FD_BACKEND_PREFILL:
+      return fd_prefill(q, n_q, causal, kv, out, lse, B, Hq, Hkv, seq_lens, max_seq_len, D, scale, workspace,
+                        workspace_bytes, stream);
+    default:
+      return n_q < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 ? FD_ERR_INVALID_ARG : FD_ERR_UNSUPPORTED;
+  }
 }
 
 fd_status fd_split_partial(const float* q, const fd_kv_desc* kv, int32_t B, int32_t Hq, int32_t Hkv,

@@ -1,0 +1,479 @@
+// fd_prefill.cu -- attention for many query rows per sequence (prefill, or a
+// long window of new tokens), on the 5th-generation tensor cores.
+//
+// The rows are the last n_q tokens of each sequence, whose keys are already in
+// the cache; with causal masking row i sees keys t < L_b - (n_q - 1 - i)
+// (the same operation as fd_decode_rows, for windows too long to serve as
+// virtual heads).  "FlashDecoding and split-KV", section "Walking through it",
+// contrasts this phase -- many query rows, FlashAttention's tiling along the
+// query axis -- with decode.
+//
+// One CTA per (batch, query head, tile of kPrefillRows = 128 query rows), six
+// warps:
+//   warp 0    TMA producer: 64-key K and V tiles (16-row x 128-byte boxes, the
+//             128-byte swizzle) into a 2-stage ring;
+//   warp 1    allocates 256 TMEM columns and issues tcgen05.mma from one thread:
+//             S = Q K^T (M=128, N=64, K=128) into one of two TMEM buffers, then
+//             O += P V (M=128, N=128, K=64) into the TMEM accumulator;
+//   warps 2-5 softmax: thread = query row = TMEM lane; reads S with tcgen05.ld,
+//             masks, keeps the running max and sum, writes P to shared memory,
+//             rescales O in TMEM when the max moves, and finally writes O / l.
+// K and V are bf16, so the products are exact once q and p are bf16: q (times
+// scale*log2 e) and p are split into bf16 hi + lo parts and each product is
+// issued twice (hi, then lo) into the same fp32 accumulator -- two MMAs buy
+// fp32-level accuracy.  The online softmax rescales lazily: the reference max
+// moves only when a score exceeds it by kTau (base 2), so p <= 2^kTau.
+#include <cuda_bf16.h>
+
+#include "fd_device.cuh"
+#include "fd_prefill.h"
+
+namespace fdk {
+namespace {
+
+constexpr int kM = kPrefillRows;   // query rows per CTA (TMEM lanes)
+constexpr int kN = kPrefillKeys;   // keys per tile
+constexpr int kD = 128;            // head dim
+constexpr int kThreads = 192;
+constexpr float kTau = 8.0f;
+constexpr float kLn2f = 0.6931471805599453f;
+
+// shared memory (byte offsets from a 1024-aligned base)
+constexpr uint32_t kQhi = 0;                  // [2 col blocks][128 rows][128 B] bf16
+constexpr uint32_t kQlo = 32768;
+constexpr uint32_t kStage0 = 65536;           // per stage: K [2][64][128 B] then V [2][64][128 B]
+constexpr uint32_t kStageBytes = 32768;
+constexpr uint32_t kTileBytes = 16384;
+constexpr uint32_t kPhi = 131072;             // [128 rows][128 B] bf16 (64 keys)
+constexpr uint32_t kPlo = 147456;
+constexpr uint32_t kBarOff = 196608;          // after a 32 KB guard region
+constexpr uint32_t kSmemBytes = kBarOff + 128;
+constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+constexpr uint32_t kTmemCols = 256;           // S buffers at columns 0 and 64, O at 128
+
+// ---------------------------------------------------------------- tcgen05
+// Shared-memory matrix descriptor (sm_100 family): start address, leading and
+// stride byte offsets (all >> 4), version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// x = hi + lo in bf16, packed as a pair (x0's part in the low half).
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 r = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Byte offset of 16-byte chunk `c` (8 bf16) of row `r` in a [rows][128 B] block
+// with the 128-byte swizzle (block base 1024-aligned).
+__device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) { return r * 128u + (((c ^ r) & 7u) << 4); }
+
+__device__ __forceinline__ int32_t row_keys(const PrefillParams& p, int32_t L, int32_t qi) {
+  if (qi >= p.n_q) return 0;
+  if (!p.causal) return L;
+  const int32_t lim = L - (p.n_q - 1 - qi);
+  return lim < 0 ? 0 : (lim > L ? L : lim);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fd_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                      const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* kv_full = bars;        // [2]
+  uint64_t* kv_empty = bars + 2;   // [2]
+  uint64_t* s_full = bars + 4;     // [2]
+  uint64_t* p_full = bars + 6;
+  uint64_t* o_done = bars + 7;
+  uint64_t* q_ready = bars + 8;
+  uint64_t* drain = bars + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 96);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 100);
+
+  const int32_t b = blockIdx.z, h = blockIdx.y;
+  const int32_t m0 = (int32_t)(gridDim.x - 1 - blockIdx.x) * kM;  // longest causal tiles first
+  const int32_t kvh = h / p.g;
+  int32_t L = p.seq_lens ? __ldg(p.seq_lens + b) : p.max_len;
+  L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
+  const int32_t last_row = (p.n_q - m0 < kM ? p.n_q - m0 : kM) - 1;
+  const int32_t keys_max = row_keys(p, L, m0 + last_row);  // rows' limits grow with the row
+  const int32_t n_tiles = (keys_max + kN - 1) / kN;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(kv_full + i, 1);
+      mbar_init(kv_empty + i, 1);
+      mbar_init(s_full + i, 1);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(q_ready, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int32_t issued = 0;
+    for (int32_t j = 0; j < n_tiles && ok; ++j) {
+      const uint32_t stage = j & 1, use = (uint32_t)j >> 1;
+      if (lane == 0 && (*abort_flag || !mbar_wait(kv_empty + stage, (use & 1) ^ 1))) ok = false;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const int32_t t0 = j * kN;
+      const int32_t nvalid = L - t0 < kN ? L - t0 : kN;
+      const int32_t tok = t0 + 16 * lane;
+      bool mine = 16 * lane < nvalid;
+      int32_t row = tok, z = b * p.Hkv + kvh;
+      if (p.paged && mine) {
+        const int32_t page = __ldg(p.block_table + (size_t)b * p.max_pages + tok / p.page_size);
+        if (page < 0 || page >= p.num_pages) {
+          atomicOr(p.err, kErrBadIndex);
+          mine = false;
+        }
+        row = tok % p.page_size;
+        z = page * p.Hkv + kvh;
+      }
+      const unsigned issue = __ballot_sync(0xffffffffu, mine);
+      if (lane == 0) mbar_arrive_expect_tx(kv_full + stage, (uint32_t)__popc(issue) * 4u * 2048u);
+      __syncwarp();
+      if (mine) {
+        uint8_t* kdst = smem + kStage0 + stage * kStageBytes + lane * 2048;
+        uint8_t* vdst = kdst + kTileBytes;
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          tma_load_3d(kdst + blk * 8192, &tmap_k, kv_full + stage, blk * 64, row, z);
+          tma_load_3d(vdst + blk * 8192, &tmap_v, kv_full + stage, blk * 64, row, z);
+        }
+      }
+      issued = j + 1;
+    }
+    if (!ok) *abort_flag = 1;
+    // do not leave while this warp's copies may still be landing
+    if (lane == 0) {
+      const int32_t first = issued > 2 ? issued - 2 : 0;
+      for (int32_t j = first; j < issued; ++j)
+        if (!mbar_wait(kv_full + (j & 1), ((uint32_t)j >> 1) & 1)) atomicOr(p.err, kErrTimeout);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0 && n_tiles > 0) {
+      constexpr uint32_t idS = instr_desc(kM, kN, false);
+      constexpr uint32_t idO = instr_desc(kM, kD, true);
+      if (!mbar_wait(q_ready, 0)) ok = false;
+      tc_fence_after();
+      for (int32_t j = 0; j <= n_tiles && ok; ++j) {
+        if (j < n_tiles) {
+          const uint32_t stage = j & 1;
+          if (*abort_flag || !mbar_wait(kv_full + stage, ((uint32_t)j >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + (uint32_t)(j & 1) * kN;
+          const uint32_t kt = sbase + kStage0 + stage * kStageBytes;
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t qt = sbase + (part ? kQlo : kQhi);
+#pragma unroll
+            for (int s = 0; s < kD / 16; ++s) {
+              const uint32_t off = (uint32_t)(s >> 2) * 8192u + (uint32_t)(s & 3) * 32u;
+              const uint64_t a = smem_desc(qt + (uint32_t)(s >> 2) * 16384u + (uint32_t)(s & 3) * 32u, 0, 1024);
+              const uint64_t bd = smem_desc(kt + off, 0, 1024);
+              umma(d, a, bd, idS, (part | s) != 0);
+            }
+          }
+          umma_commit(s_full + (j & 1));
+        }
+        if (j >= 1) {
+          const int32_t jj = j - 1;
+          const uint32_t stage = jj & 1;
+          if (*abort_flag || !mbar_wait(p_full, (uint32_t)jj & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vt = sbase + kStage0 + stage * kStageBytes + kTileBytes;
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t pt = sbase + (part ? kPlo : kPhi);
+#pragma unroll
+            for (int kk = 0; kk < kN / 16; ++kk) {
+              const uint64_t a = smem_desc(pt + (uint32_t)kk * 32u, 0, 1024);
+              const uint64_t bd = smem_desc(vt + (uint32_t)kk * 2048u, 8192, 1024);
+              umma(tmem + 128, a, bd, idO, (jj | part | kk) != 0);
+            }
+          }
+          umma_commit(o_done);
+          umma_commit(kv_empty + stage);
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.err, kErrTimeout);
+      }
+      // every MMA this thread issued has finished before TMEM is released
+      umma_commit(drain);
+      if (!mbar_wait(drain, 0)) atomicOr(p.err, kErrTimeout);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int32_t quarter = warp & 3;
+    const int32_t r = quarter * 32 + lane;  // query row in the tile = TMEM lane
+    const int32_t qi = m0 + r;
+    const int32_t lim = row_keys(p, L, qi);
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+    // q row, times scale*log2(e), as bf16 hi / lo in the swizzled A layout
+    {
+      const float* qrow = p.q + (((size_t)b * p.Hq + h) * p.n_q + (qi < p.n_q ? qi : 0)) * kD;
+#pragma unroll 4
+      for (int c = 0; c < kD / 8; ++c) {
+        float x[8];
+        if (qi < p.n_q) {
+          const float4 a0 = __ldg(reinterpret_cast<const float4*>(qrow) + 2 * c);
+          const float4 a1 = __ldg(reinterpret_cast<const float4*>(qrow) + 2 * c + 1);
+          x[0] = a0.x; x[1] = a0.y; x[2] = a0.z; x[3] = a0.w;
+          x[4] = a1.x; x[5] = a1.y; x[6] = a1.z; x[7] = a1.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split2(x[2 * e] * p.qk_scale, x[2 * e + 1] * p.qk_scale, hi[e], lo[e]);
+        const uint32_t off = (uint32_t)(c >> 3) * 16384u + swz((uint32_t)r, (uint32_t)(c & 7));
+        sts128(sbase + kQhi + off, hi[0], hi[1], hi[2], hi[3]);
+        sts128(sbase + kQlo + off, lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_ready);
+
+    // A failed wait never leaves the loop early (the named barrier below needs
+    // all 128 threads): later waits are skipped and the output is flagged.
+    float mref = -INFINITY, l = 0.f;
+    for (int32_t j = 0; j < n_tiles; ++j) {
+      if (ok && (*abort_flag || !mbar_wait(s_full + (j & 1), ((uint32_t)j >> 1) & 1))) ok = false;
+      tc_fence_after();
+      float s[kN];
+      {
+        float a[32];
+        tmem_ld32(trow + (uint32_t)(j & 1) * kN, a);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) s[c] = a[c];
+        tmem_ld32(trow + (uint32_t)(j & 1) * kN + 32, a);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) s[32 + c] = a[c];
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kN; ++c) {
+        s[c] = j * kN + c < lim ? s[c] : -INFINITY;
+        mx = fmaxf(mx, s[c]);
+      }
+      const bool rescale = mx > mref + kTau;
+      float alpha = 1.f;
+      if (rescale) {
+        const float mn = fmaxf(mref, mx);
+        alpha = mref == -INFINITY ? 0.f : exp2f(mref - mn);
+        mref = mn;
+      }
+      const float base = mref == -INFINITY ? 0.f : mref;
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kN; ++c) {
+        s[c] = exp2f(s[c] - base);
+        sum += s[c];
+      }
+      l = l * alpha + sum;
+      // P and O are free once the previous tile's P.V has completed
+      if (j >= 1) {
+        if (ok && (*abort_flag || !mbar_wait(o_done, (uint32_t)(j - 1) & 1))) ok = false;
+        tc_fence_after();
+        // tcgen05.ld / st are warp-collective (.sync.aligned): the whole warp
+        // rescales when any of its rows must, the others with alpha = 1
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c4 = 0; c4 < kD / 32; ++c4) {
+            float o[32];
+            tmem_ld32(trow + 128 + (uint32_t)c4 * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(trow + 128 + (uint32_t)c4 * 32, o);
+          }
+        }
+      }
+      if (j == n_tiles - 1 && L - j * kN < kN) {
+        // keys past L in the last tile get p = 0, but 0 * NaN is NaN: zero those V rows
+        const uint32_t stage = j & 1;
+        if (ok && (*abort_flag || !mbar_wait(kv_full + stage, ((uint32_t)j >> 1) & 1))) ok = false;
+        const int32_t nvalid = L - j * kN;
+        const uint32_t vt = sbase + kStage0 + stage * kStageBytes + kTileBytes;
+        const int32_t tid2 = tid - 64;
+        for (int32_t idx = tid2; idx < (kN - nvalid) * 16; idx += 128) {
+          const uint32_t row = (uint32_t)(nvalid + idx / 16), c = (uint32_t)(idx % 16);
+          sts128(vt + (c >> 3) * 8192u + row * 128u + ((c & 7u) << 4), 0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < kN / 8; ++c) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split2(s[8 * c + 2 * e], s[8 * c + 2 * e + 1], hi[e], lo[e]);
+        const uint32_t off = swz((uint32_t)r, (uint32_t)c);
+        sts128(sbase + kPhi + off, hi[0], hi[1], hi[2], hi[3]);
+        sts128(sbase + kPlo + off, lo[0], lo[1], lo[2], lo[3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      named_barrier(1, 128);  // every softmax thread's P and V stores precede the arrival
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    // ---- epilogue: out = O / l, lse = ln(sum of exp)
+    // n_tiles is the same for the whole CTA, so the collective loads below are
+    // executed by every lane or by none
+    const bool have = n_tiles > 0;
+    if (have && ok && (*abort_flag || !mbar_wait(o_done, (uint32_t)(n_tiles - 1) & 1))) ok = false;
+    if (have) tc_fence_after();
+    float* orow = p.out + (((size_t)b * p.Hq + h) * p.n_q + qi) * kD;
+    const float inv = l > 0.f && ok ? 1.f / l : 0.f;
+#pragma unroll 1
+    for (int c4 = 0; c4 < kD / 32; ++c4) {
+      float o[32];
+      if (have) {
+        tmem_ld32(trow + 128 + (uint32_t)c4 * 32, o);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0.f;
+      }
+      if (qi < p.n_q) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(orow + c4 * 32 + i) =
+              make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+      }
+    }
+    if (qi < p.n_q && p.lse)
+      p.lse[((size_t)b * p.Hq + h) * p.n_q + qi] = l > 0.f ? (mref + log2f(l)) * kLn2f : -INFINITY;
+    if (!ok) {
+      *abort_flag = 1;
+      atomicOr(p.err, kErrTimeout);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                           cudaStream_t stream) {
+  static int configured = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured != dev) {
+    e = cudaFuncSetAttribute(fd_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    configured = dev;
+  }
+  const dim3 grid((unsigned)((p.n_q + kM - 1) / kM), (unsigned)p.Hq, (unsigned)p.B);
+  fd_prefill_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace fdk

@@ -1,0 +1,30 @@
+// fd_prefill.h -- parameters of the many-row (prefill) attention kernel,
+// shared by the host entry points and the kernel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fdk {
+
+struct PrefillParams {
+  const float* q;              // [B, Hq, n_q, D] fp32
+  float* out;                  // [B, Hq, n_q, D] fp32
+  float* lse;                  // [B, Hq, n_q] natural log, or null
+  const int32_t* seq_lens;     // [B] keys per sequence (the n_q rows are its last n_q tokens), or null
+  const int32_t* block_table;  // paged: [B, max_pages]
+  unsigned* err;               // error word (timeouts, bad pages)
+  int32_t B, Hq, Hkv, g, n_q, max_len, causal;
+  int32_t paged, page_size, max_pages, num_pages;
+  float qk_scale;              // scale * log2(e)
+};
+
+// Query rows per CTA and keys per tile of the prefill kernel.
+constexpr int kPrefillRows = 128;
+constexpr int kPrefillKeys = 64;
+
+cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                           cudaStream_t stream);
+
+}  // namespace fdk

@@ -17,7 +17,7 @@ import numpy as np
 
 __all__ = [
     "FdError", "KvDesc", "library_path", "load_library", "workspace_bytes", "split_size", "plan_pieces",
-    "Workspace", "decode", "decode_rows", "append_decode", "decode_host", "decode_static", "split_partial", "combine", "workspace_status",
+    "Workspace", "decode", "decode_rows", "append_decode", "prefill", "attend", "attend_backend", "decode_host", "decode_static", "split_partial", "combine", "workspace_status",
 ]
 
 FD_OK, FD_ERR_INVALID_ARG, FD_ERR_UNSUPPORTED, FD_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3
@@ -89,6 +89,12 @@ def load_library(path: Optional[str] = None):
                                               c_i32, f32, c_i32, vp, c_sz, vp]),
             "fd_append_decode": (ctypes.c_int, [vp, vp, vp, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32, c_i32, f32,
                                                 c_i32, vp, c_sz, vp]),
+            "fd_prefill": (ctypes.c_int, [vp, c_i32, c_i32, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32, c_i32, f32,
+                                          vp, c_sz, vp]),
+            "fd_attend": (ctypes.c_int, [vp, c_i32, c_i32, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32, c_i32, f32,
+                                         c_i32, vp, c_sz, vp, ctypes.POINTER(c_i32)]),
+            "fd_attend_backend": (c_i32, [c_i32, c_i32, c_i32, c_i32, c_i32]),
+            "fd_backend_name": (ctypes.c_char_p, [c_i32]),
             "fd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "fd_version": (c_i32, []),
         }
@@ -325,6 +331,69 @@ def append_decode(q, k, v, k_new, v_new, *, seq_lens=None, max_seq_len=None, blo
                                  _stream_handle(q.device, stream))
     _check(st, "fd_append_decode")
     return out, lse
+
+
+def _rows_args(q, k, v, block_table, seq_lens, max_seq_len, scale, out, lse, return_lse):
+    torch = _torch()
+    _need_cuda(q, "q", torch.float32)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, Hq, n_q, D]")
+    kv = _kv_desc(k, v, block_table)
+    B, Hq, n_q, D = q.shape
+    if max_seq_len is None:
+        max_seq_len = k.shape[2] if block_table is None else block_table.shape[1] * k.shape[2]
+    if seq_lens is not None:
+        _need_cuda(seq_lens, "seq_lens", torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, n_q, D), dtype=torch.float32, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, n_q), dtype=torch.float32, device=q.device)
+    return kv, B, Hq, n_q, D, max_seq_len, scale, out, lse
+
+
+def prefill(q, k, v, *, causal=True, seq_lens=None, max_seq_len=None, block_table=None, scale=None, out=None,
+            lse=None, return_lse=True, workspace: Optional[Workspace] = None, stream=None):
+    """``fd_prefill``: the ``decode_rows`` operation for long windows, on tcgen05 query tiles."""
+    kv, B, Hq, n_q, D, max_seq_len, scale, out, lse = _rows_args(q, k, v, block_table, seq_lens, max_seq_len,
+                                                                scale, out, lse, return_lse)
+    ws = workspace or _default_workspace(q.device)
+    buf = ws.get(256, q.device)
+    st = _lib().fd_prefill(q.data_ptr(), int(n_q), int(bool(causal)), ctypes.byref(kv), out.data_ptr(),
+                           lse.data_ptr() if lse is not None else None, B, Hq, k.shape[1],
+                           seq_lens.data_ptr() if seq_lens is not None else None, int(max_seq_len), D, float(scale),
+                           buf.data_ptr(), buf.numel(), _stream_handle(q.device, stream))
+    _check(st, "fd_prefill")
+    return out, lse
+
+
+def attend_backend(n_q, Hq, Hkv, D, kv_dtype="bf16") -> str:
+    """Name of the backend ``attend`` would run (``fd_attend_backend``)."""
+    dt = {"bf16": FD_BF16, "f32": FD_F32}[kv_dtype]
+    return _lib().fd_backend_name(_lib().fd_attend_backend(int(n_q), int(Hq), int(Hkv), int(D), dt)).decode()
+
+
+def attend(q, k, v, *, causal=True, seq_lens=None, max_seq_len=None, block_table=None, scale=None,
+           n_splits=FD_SPLITS_AUTO, out=None, lse=None, return_lse=True, workspace: Optional[Workspace] = None,
+           stream=None):
+    """``fd_attend``: phase dispatch for q ``[B, Hq, n_q, D]``; returns ``(out, lse, backend name)``."""
+    kv, B, Hq, n_q, D, max_seq_len, scale, out, lse = _rows_args(q, k, v, block_table, seq_lens, max_seq_len,
+                                                                scale, out, lse, return_lse)
+    Hkv = k.shape[1]
+    lib = _lib()
+    be = lib.fd_attend_backend(int(n_q), Hq, Hkv, D, kv.dtype)
+    need = 256 if be == 2 else workspace_bytes(B, Hq * n_q, Hkv, D, n_splits)
+    ws = workspace or _default_workspace(q.device)
+    buf = ws.get(need, q.device)
+    chosen = ctypes.c_int32(-1)
+    st = lib.fd_attend(q.data_ptr(), int(n_q), int(bool(causal)), ctypes.byref(kv), out.data_ptr(),
+                       lse.data_ptr() if lse is not None else None, B, Hq, Hkv,
+                       seq_lens.data_ptr() if seq_lens is not None else None, int(max_seq_len), D, float(scale),
+                       int(n_splits), buf.data_ptr(), buf.numel(), _stream_handle(q.device, stream),
+                       ctypes.byref(chosen))
+    _check(st, "fd_attend")
+    return out, lse, lib.fd_backend_name(chosen.value).decode()
 
 
 def decode_static(q, k, v, *, out, lse=None, seq_lens=None, max_seq_len=None, block_table=None, scale=None,

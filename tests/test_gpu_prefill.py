@@ -1,0 +1,139 @@
+"""GPU parity of ``fd_prefill`` (tcgen05 query tiles) and of the ``fd_attend`` phase dispatch.
+
+Same operation and tolerance as ``fd_decode_rows``: ``|gpu - ref| <= 1e-4 * (1 + |ref|)``
+against the oracle's ``decode_rows``, ``lse = -inf`` exactly for rows without keys,
+and padding poisoned with NaN must not change one output bit.
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import split_kv_decode_fd_gb300 as fd
+from workloads import make_case, poison_padding, small_spec
+
+from test_gpu_parity import assert_close, np64
+
+pytestmark = pytest.mark.gpu
+
+
+def window_q(case, n_q, seed=5):
+    s = case.spec
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    return torch.randn((s.B, s.Hq, n_q, s.D), generator=gen, device="cuda") * s.q_gain
+
+
+def oracle_rows(case, q, causal):
+    bt = None if case.block_table is None else case.block_table.cpu().numpy()
+    return oracle.decode_rows(np64(q), np64(case.k), np64(case.v), case.spec.scale, causal=causal,
+                              seq_lens=case.lengths, max_seq_len=case.max_seq_len, block_table=bt,
+                              page_size=case.spec.page_size if bt is not None else None)
+
+
+def run_prefill(case, q, causal, **kw):
+    return fd.prefill(q, case.k, case.v, causal=causal, seq_lens=case.seq_lens, max_seq_len=case.max_seq_len,
+                      block_table=case.block_table, scale=case.spec.scale, **kw)
+
+
+SPECS = [
+    (small_spec("mha_L300", 1, 2, 2, 128, 300), 300),
+    (small_spec("gqa4_ragged", 2, 8, 2, 128, 700, lengths="uniform:1:700"), 200),   # some L_b < n_q
+    (small_spec("gqa8_prefix", 2, 16, 2, 128, 900, lengths="uniform:400:900"), 129),
+    (small_spec("peaked", 1, 4, 1, 128, 520, q_gain=6.0), 260),
+    (small_spec("paged16_gqa4", 3, 8, 2, 128, 600, layout="paged", page_size=16, lengths="uniform:1:600"), 150),
+    (small_spec("paged64_mha", 2, 2, 2, 128, 500, layout="paged", page_size=64, lengths="uniform:200:500"), 64),
+]
+
+
+@pytest.mark.parametrize("spec,n_q", SPECS, ids=lambda x: getattr(x, "name", str(x)))
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_vs_oracle(spec, n_q, causal):
+    case = make_case(spec, "cuda")
+    q = window_q(case, n_q)
+    ws = fd.Workspace()
+    out, lse = run_prefill(case, q, causal, workspace=ws)
+    ref_out, ref_lse = oracle_rows(case, q, causal)
+    torch.cuda.synchronize()
+    assert fd.workspace_status(ws) == 0
+    assert_close(np64(out), ref_out, "out")
+    assert_close(np64(lse), ref_lse, "lse")
+
+
+@pytest.mark.parametrize("n_q", [1, 7, 64])
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+def test_prefill_agrees_with_decode_rows(n_q, layout):
+    spec = small_spec("agree", 3, 8, 2, 128, 800, layout=layout, lengths="uniform:64:800")
+    case = make_case(spec, "cuda")
+    q = window_q(case, n_q, seed=8)
+    a_out, a_lse = run_prefill(case, q, True)
+    b_out, b_lse = fd.decode_rows(q, case.k, case.v, causal=True, seq_lens=case.seq_lens,
+                                  max_seq_len=case.max_seq_len, block_table=case.block_table, scale=spec.scale)
+    torch.cuda.synchronize()
+    assert_close(np64(a_out), np64(b_out).astype(np.float64), "out vs decode_rows")
+    assert_close(np64(a_lse), np64(b_lse).astype(np.float64), "lse vs decode_rows")
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+def test_prefill_padding_is_bit_exact(layout):
+    spec = small_spec("poison", 3, 4, 2, 128, 500, layout=layout, lengths="uniform:1:500")
+    case = make_case(spec, "cuda")
+    q = window_q(case, 180, seed=4)
+    bad = poison_padding(case)
+    for causal in (True, False):
+        a = run_prefill(case, q, causal)
+        b = run_prefill(bad, q, causal)
+        torch.cuda.synchronize()
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_prefill_long_prompt_sampled():
+    """A 4096-token causal prompt over a 4096-key cache (B=1, Hq=32, Hkv=8): sampled rows."""
+    spec = small_spec("prompt4k", 1, 32, 8, 128, 4096)
+    case = make_case(spec, "cuda")
+    n_q = 4096
+    q = window_q(case, n_q, seed=11)
+    out, lse = run_prefill(case, q, True)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    r = np.random.default_rng(0)
+    rows = [(int(r.integers(0, 32)), int(r.integers(0, n_q))) for _ in range(12)] + [(0, 0), (31, n_q - 1)]
+    g = 4
+    for h, i in rows:
+        lim = oracle.row_key_limit(4096, n_q, i, True)
+        kvh = oracle.kv_head_for(h, g)
+        ro, rl = oracle.attend_row(np64(q[0, h, i]), np64(case.k[0, kvh, :lim]), np64(case.v[0, kvh, :lim]),
+                                   spec.scale)
+        assert_close(np64(out[0, h, i]), ro, f"out[{h},{i}]")
+        assert_close(np.array([float(lse[0, h, i])]), np.array([rl]), f"lse[{h},{i}]")
+
+
+def test_prefill_rejects_what_it_does_not_cover():
+    for spec in (small_spec("d64", 1, 2, 2, 64, 64), small_spec("f32", 1, 2, 2, 128, 64, kv_dtype="f32")):
+        case = make_case(spec, "cuda")
+        q = window_q(case, 80)
+        with pytest.raises(RuntimeError, match="fd_prefill"):
+            run_prefill(case, q, True)
+
+
+@pytest.mark.parametrize("n_q,hq,hkv,dtype,expect", [
+    (1, 8, 2, "bf16", "decode"),
+    (4, 8, 2, "bf16", "decode_rows"),     # 4 rows x 4 heads = 16 per KV head
+    (5, 8, 2, "bf16", "prefill"),
+    (300, 8, 2, "bf16", "prefill"),
+    (20, 4, 4, "f32", "decode_rows"),     # no prefill kernel for fp32 caches
+])
+def test_attend_dispatch(n_q, hq, hkv, dtype, expect):
+    assert fd.attend_backend(n_q, hq, hkv, 128, dtype).startswith(expect)
+    spec = small_spec("attend", 2, hq, hkv, 128, 400, kv_dtype=dtype, lengths="uniform:300:400")
+    case = make_case(spec, "cuda")
+    q = window_q(case, n_q, seed=2)
+    out, lse, name = fd.attend(q, case.k, case.v, causal=True, seq_lens=case.seq_lens,
+                               max_seq_len=case.max_seq_len, scale=spec.scale)
+    torch.cuda.synchronize()
+    assert name.startswith(expect)
+    ref_out, ref_lse = oracle_rows(case, q, True)
+    assert_close(np64(out), ref_out, "out")
+    assert_close(np64(lse), ref_lse, "lse")
