@@ -8,16 +8,23 @@
 // contrasts this phase -- many query rows, FlashAttention's tiling along the
 // query axis -- with decode.
 //
-// One CTA per (batch, query head, tile of kPrefillRows = 128 query rows), six
-// warps:
+// One CTA per (batch, pair of query heads of one GQA group -- or one head when
+// the group size is odd --, tile of kPrefillRows = 128 query rows), ten warps:
 //   warp 0    TMA producer: 64-key K and V tiles (16-row x 128-byte boxes, the
-//             128-byte swizzle) into a 2-stage ring;
-//   warp 1    allocates 256 TMEM columns and issues tcgen05.mma from one thread:
-//             S = Q K^T (M=128, N=64, K=128) into one of two TMEM buffers, then
-//             O += P V (M=128, N=128, K=64) into the TMEM accumulator;
-//   warps 2-5 softmax: thread = query row = TMEM lane; reads S with tcgen05.ld,
-//             masks, keeps the running max and sum, writes P to shared memory,
-//             rescales O in TMEM when the max moves, and finally writes O / l.
+//             128-byte swizzle) into a 2-stage ring, shared by both heads;
+//   warp 1    allocates all 512 TMEM columns and issues tcgen05.mma from one
+//             thread, per head: S = Q K^T (M=128, N=64, K=128) into one of two
+//             TMEM buffers, then O += P V (M=128, N=128, K=64) into its TMEM
+//             accumulator;
+//   warps 2-5 and 6-9: the two heads' softmax groups, which take turns with
+//             the tensor core (two warps per SM sub-partition hide each
+//             other's latency).  Thread = query row = TMEM lane; reads S with tcgen05.ld,
+//             masks, keeps the running max and sum, writes P (bf16 hi and lo)
+//             back over its own S columns with tcgen05.st, rescales O in TMEM
+//             when the max moves, and finally writes O / l.
+// P . V takes A = P straight from TMEM, so the softmax of tile j never waits
+// for P . V of tile j - 1 (that one reads the other S buffer) except to
+// rescale O.
 // K and V are bf16, so the products are exact once q and p are bf16: q (times
 // scale*log2 e) and p are split into bf16 hi + lo parts and each product is
 // issued twice (hi, then lo) into the same fp32 accumulator -- two MMAs buy
@@ -34,22 +41,21 @@ namespace {
 constexpr int kM = kPrefillRows;   // query rows per CTA (TMEM lanes)
 constexpr int kN = kPrefillKeys;   // keys per tile
 constexpr int kD = 128;            // head dim
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;      // producer, MMA, two softmax groups of four warps
 constexpr float kTau = 8.0f;
 constexpr float kLn2f = 0.6931471805599453f;
 
 // shared memory (byte offsets from a 1024-aligned base)
-constexpr uint32_t kQhi = 0;                  // [2 col blocks][128 rows][128 B] bf16
+constexpr uint32_t kQhi = 0;                  // per group: [2 col blocks][128 rows][128 B] bf16, hi then lo
 constexpr uint32_t kQlo = 32768;
-constexpr uint32_t kStage0 = 65536;           // per stage: K [2][64][128 B] then V [2][64][128 B]
+constexpr uint32_t kQGroupBytes = 65536;
+constexpr uint32_t kStage0 = 131072;          // per stage: K [2][64][128 B] then V [2][64][128 B]
 constexpr uint32_t kStageBytes = 32768;
 constexpr uint32_t kTileBytes = 16384;
-constexpr uint32_t kPhi = 131072;             // [128 rows][128 B] bf16 (64 keys)
-constexpr uint32_t kPlo = 147456;
-constexpr uint32_t kBarOff = 196608;          // after a 32 KB guard region
-constexpr uint32_t kSmemBytes = kBarOff + 128;
+constexpr uint32_t kBarOff = 196608;
+constexpr uint32_t kSmemBytes = kBarOff + 256;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
-constexpr uint32_t kTmemCols = 256;           // S buffers at columns 0 and 64, O at 128
+constexpr uint32_t kTmemCols = 512;           // per group (256 each): S / P at +0 and +64, O at +128
 
 // ---------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor (sm_100 family): start address, leading and
@@ -75,6 +81,16 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// A from tensor memory (M rows in lanes, two bf16 of K per 32-bit column).
+__device__ __forceinline__ void umma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 
@@ -121,6 +137,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
 // x = hi + lo in bf16, packed as a pair (x0's part in the low half).
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
@@ -153,19 +180,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_addr(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* kv_full = bars;        // [2]
-  uint64_t* kv_empty = bars + 2;   // [2]
-  uint64_t* s_full = bars + 4;     // [2]
-  uint64_t* p_full = bars + 6;
-  uint64_t* o_done = bars + 7;
-  uint64_t* q_ready = bars + 8;
-  uint64_t* drain = bars + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 96);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 100);
+  uint64_t* kv_full = bars;        // [2 stages]
+  uint64_t* kv_empty = bars + 2;   // [2 stages]
+  // Every barrier a waiter might fall behind on alternates between two
+  // instances (tile j uses instance j % 2, phase j / 2), so that no barrier can
+  // complete two phases ahead of a parity wait: S of tile j+1 is issued before
+  // the MMA thread waits for P of tile j, so a fast softmax group may finish
+  // tiles j and j+1 meanwhile.
+  uint64_t* s_full = bars + 4;     // [2 groups][2]
+  uint64_t* p_full = bars + 8;     // [2 groups][2]
+  uint64_t* o_done = bars + 12;    // [2 groups][2]
+  uint64_t* o_final = bars + 16;   // [2 groups]: the group's last P.V has completed (one phase)
+  uint64_t* q_ready = bars + 18;
+  uint64_t* drain = bars + 19;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 160);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 164);
 
-  const int32_t b = blockIdx.z, h = blockIdx.y;
+  // Two query heads of one GQA group share the CTA (and every K/V tile) when
+  // the group size is even; otherwise the second softmax group idles.
+  const int32_t ngroups = (p.g % 2 == 0) ? 2 : 1;
+  const int32_t b = blockIdx.z, h0 = blockIdx.y * ngroups;
   const int32_t m0 = (int32_t)(gridDim.x - 1 - blockIdx.x) * kM;  // longest causal tiles first
-  const int32_t kvh = h / p.g;
+  const int32_t kvh = h0 / p.g;
   int32_t L = p.seq_lens ? __ldg(p.seq_lens + b) : p.max_len;
   L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
   const int32_t last_row = (p.n_q - m0 < kM ? p.n_q - m0 : kM) - 1;
@@ -176,11 +212,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(kv_full + i, 1);
       mbar_init(kv_empty + i, 1);
-      mbar_init(s_full + i, 1);
+      mbar_init(o_final + i, 1);
     }
-    mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
-    mbar_init(q_ready, 4);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(s_full + i, 1);
+      mbar_init(p_full + i, 4);
+      mbar_init(o_done + i, 1);
+    }
+    mbar_init(q_ready, 4 * ngroups);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -259,41 +298,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t d = tmem + (uint32_t)(j & 1) * kN;
           const uint32_t kt = sbase + kStage0 + stage * kStageBytes;
+          for (int G = 0; G < ngroups; ++G) {
+            const uint32_t d = tmem + (uint32_t)G * 256u + (uint32_t)(j & 1) * kN;
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            const uint32_t qt = sbase + (part ? kQlo : kQhi);
+            for (int part = 0; part < 2; ++part) {
+              const uint32_t qt = sbase + (uint32_t)G * kQGroupBytes + (part ? kQlo : kQhi);
 #pragma unroll
-            for (int s = 0; s < kD / 16; ++s) {
-              const uint32_t off = (uint32_t)(s >> 2) * 8192u + (uint32_t)(s & 3) * 32u;
-              const uint64_t a = smem_desc(qt + (uint32_t)(s >> 2) * 16384u + (uint32_t)(s & 3) * 32u, 0, 1024);
-              const uint64_t bd = smem_desc(kt + off, 0, 1024);
-              umma(d, a, bd, idS, (part | s) != 0);
+              for (int s8 = 0; s8 < kD / 16; ++s8) {
+                const uint32_t off = (uint32_t)(s8 >> 2) * 8192u + (uint32_t)(s8 & 3) * 32u;
+                const uint64_t a = smem_desc(qt + (uint32_t)(s8 >> 2) * 16384u + (uint32_t)(s8 & 3) * 32u, 0, 1024);
+                const uint64_t bd = smem_desc(kt + off, 0, 1024);
+                umma(d, a, bd, idS, (part | s8) != 0);
+              }
             }
+            umma_commit(s_full + G * 2 + (j & 1));
           }
-          umma_commit(s_full + (j & 1));
         }
         if (j >= 1) {
           const int32_t jj = j - 1;
           const uint32_t stage = jj & 1;
-          if (*abort_flag || !mbar_wait(p_full, (uint32_t)jj & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           const uint32_t vt = sbase + kStage0 + stage * kStageBytes + kTileBytes;
-#pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            const uint32_t pt = sbase + (part ? kPlo : kPhi);
-#pragma unroll
-            for (int kk = 0; kk < kN / 16; ++kk) {
-              const uint64_t a = smem_desc(pt + (uint32_t)kk * 32u, 0, 1024);
-              const uint64_t bd = smem_desc(vt + (uint32_t)kk * 2048u, 8192, 1024);
-              umma(tmem + 128, a, bd, idO, (jj | part | kk) != 0);
+          for (int G = 0; G < ngroups && ok; ++G) {
+            if (*abort_flag || !mbar_wait(p_full + G * 2 + (jj & 1), ((uint32_t)jj >> 1) & 1)) {
+              ok = false;
+              break;
             }
+            tc_fence_after();
+            const uint32_t pt = tmem + (uint32_t)G * 256u + (uint32_t)(jj & 1) * kN;  // P hi [0, 32), lo [32, 64)
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+#pragma unroll
+              for (int kk = 0; kk < kN / 16; ++kk) {
+                const uint64_t bd = smem_desc(vt + (uint32_t)kk * 2048u, 8192, 1024);
+                umma_tmem_a(tmem + (uint32_t)G * 256u + 128u, pt + (uint32_t)part * (kN / 2) + (uint32_t)kk * 8u, bd,
+                            idO, (jj | part | kk) != 0);
+              }
+            }
+            umma_commit(o_done + G * 2 + (jj & 1));
+            if (jj == n_tiles - 1) umma_commit(o_final + G);
           }
-          umma_commit(o_done);
+          if (!ok) break;
           umma_commit(kv_empty + stage);
         }
       }
@@ -305,13 +350,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(drain);
       if (!mbar_wait(drain, 0)) atomicOr(p.err, kErrTimeout);
     }
-  } else {
-    // ------------------------------------------------------------ softmax
+  } else if ((warp - 2) / 4 < ngroups) {
+    // ------------------------------------------------------------ softmax, group G
+    const int32_t G = (warp - 2) / 4;
+    const int32_t h = h0 + G;
     const int32_t quarter = warp & 3;
     const int32_t r = quarter * 32 + lane;  // query row in the tile = TMEM lane
     const int32_t qi = m0 + r;
     const int32_t lim = row_keys(p, L, qi);
-    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t tbase = tmem + (uint32_t)G * 256u + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t qbase = sbase + (uint32_t)G * kQGroupBytes;
+    uint64_t* my_s_full = s_full + G * 2;
     // q row, times scale*log2(e), as bf16 hi / lo in the swizzled A layout
     {
       const float* qrow = p.q + (((size_t)b * p.Hq + h) * p.n_q + (qi < p.n_q ? qi : 0)) * kD;
@@ -331,8 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) split2(x[2 * e] * p.qk_scale, x[2 * e + 1] * p.qk_scale, hi[e], lo[e]);
         const uint32_t off = (uint32_t)(c >> 3) * 16384u + swz((uint32_t)r, (uint32_t)(c & 7));
-        sts128(sbase + kQhi + off, hi[0], hi[1], hi[2], hi[3]);
-        sts128(sbase + kQlo + off, lo[0], lo[1], lo[2], lo[3]);
+        sts128(qbase + kQhi + off, hi[0], hi[1], hi[2], hi[3]);
+        sts128(qbase + kQlo + off, lo[0], lo[1], lo[2], lo[3]);
       }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -340,18 +389,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(q_ready);
 
     // A failed wait never leaves the loop early (the named barrier below needs
-    // all 128 threads): later waits are skipped and the output is flagged.
+    // all 128 threads of the group): later waits are skipped, the output flagged.
     float mref = -INFINITY, l = 0.f;
     for (int32_t j = 0; j < n_tiles; ++j) {
-      if (ok && (*abort_flag || !mbar_wait(s_full + (j & 1), ((uint32_t)j >> 1) & 1))) ok = false;
+      if (ok && (*abort_flag || !mbar_wait(my_s_full + (j & 1), ((uint32_t)j >> 1) & 1))) ok = false;
       tc_fence_after();
       float s[kN];
       {
         float a[32];
-        tmem_ld32(trow + (uint32_t)(j & 1) * kN, a);
+        tmem_ld32(tbase + (uint32_t)(j & 1) * kN, a);
 #pragma unroll
         for (int c = 0; c < 32; ++c) s[c] = a[c];
-        tmem_ld32(trow + (uint32_t)(j & 1) * kN + 32, a);
+        tmem_ld32(tbase + (uint32_t)(j & 1) * kN + 32, a);
 #pragma unroll
         for (int c = 0; c < 32; ++c) s[32 + c] = a[c];
       }
@@ -376,54 +425,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         sum += s[c];
       }
       l = l * alpha + sum;
-      // P and O are free once the previous tile's P.V has completed
-      if (j >= 1) {
-        if (ok && (*abort_flag || !mbar_wait(o_done, (uint32_t)(j - 1) & 1))) ok = false;
+      // Rescaling O needs the previous tile's P.V to have finished.  tcgen05.ld
+      // and st are warp-collective (.sync.aligned): the whole warp rescales
+      // when any of its rows must, the others with alpha = 1.  P.V of tile j-1
+      // completes phase (j-1)/2 of o_done[G][(j-1)%2]; a parity wait for it is
+      // exact although earlier phases were not waited: that barrier's previous
+      // phase (tile j-3) finished before this tile's S (issued after it, in
+      // order), and its next one (tile j+1) needs this group's P first.
+      if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+        if (ok && (*abort_flag || !mbar_wait(o_done + G * 2 + ((j - 1) & 1), ((uint32_t)(j - 1) >> 1) & 1)))
+          ok = false;
         tc_fence_after();
-        // tcgen05.ld / st are warp-collective (.sync.aligned): the whole warp
-        // rescales when any of its rows must, the others with alpha = 1
-        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-          for (int c4 = 0; c4 < kD / 32; ++c4) {
-            float o[32];
-            tmem_ld32(trow + 128 + (uint32_t)c4 * 32, o);
+        for (int c4 = 0; c4 < kD / 32; ++c4) {
+          float o[32];
+          tmem_ld32(tbase + 128 + (uint32_t)c4 * 32, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(trow + 128 + (uint32_t)c4 * 32, o);
-          }
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(tbase + 128 + (uint32_t)c4 * 32, o);
         }
       }
-      if (j == n_tiles - 1 && L - j * kN < kN) {
-        // keys past L in the last tile get p = 0, but 0 * NaN is NaN: zero those V rows
+      if (G == 0 && j == n_tiles - 1 && L - j * kN < kN) {
+        // keys past L in the last tile get p = 0, but 0 * NaN is NaN: zero those V
+        // rows (group 0 does it for both: its P.V is issued first)
         const uint32_t stage = j & 1;
         if (ok && (*abort_flag || !mbar_wait(kv_full + stage, ((uint32_t)j >> 1) & 1))) ok = false;
         const int32_t nvalid = L - j * kN;
         const uint32_t vt = sbase + kStage0 + stage * kStageBytes + kTileBytes;
-        const int32_t tid2 = tid - 64;
+        const int32_t tid2 = (warp - 2) * 32 + lane;
         for (int32_t idx = tid2; idx < (kN - nvalid) * 16; idx += 128) {
           const uint32_t row = (uint32_t)(nvalid + idx / 16), c = (uint32_t)(idx % 16);
           sts128(vt + (c >> 3) * 8192u + row * 128u + ((c & 7u) << 4), 0u, 0u, 0u, 0u);
         }
       }
+      // P over this tile's S columns: hi in [0, 32), lo in [32, 64), two keys per column
+      {
+        uint32_t hi[32], lo[32];
 #pragma unroll
-      for (int c = 0; c < kN / 8; ++c) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) split2(s[8 * c + 2 * e], s[8 * c + 2 * e + 1], hi[e], lo[e]);
-        const uint32_t off = swz((uint32_t)r, (uint32_t)c);
-        sts128(sbase + kPhi + off, hi[0], hi[1], hi[2], hi[3]);
-        sts128(sbase + kPlo + off, lo[0], lo[1], lo[2], lo[3]);
+        for (int c = 0; c < kN / 2; ++c) split2(s[2 * c], s[2 * c + 1], hi[c], lo[c]);
+        const uint32_t pt = tbase + (uint32_t)(j & 1) * kN;
+        tmem_st32u(pt, hi);
+        tmem_st32u(pt + kN / 2, lo);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the zeroed V rows, if any
       tc_fence_before();
-      named_barrier(1, 128);  // every softmax thread's P and V stores precede the arrival
-      if (lane == 0) mbar_arrive(p_full);
+      named_barrier(1 + G, 128);  // every thread of the group has stored before the arrival
+      if (lane == 0) mbar_arrive(p_full + G * 2 + (j & 1));
     }
-    // ---- epilogue: out = O / l, lse = ln(sum of exp)
-    // n_tiles is the same for the whole CTA, so the collective loads below are
-    // executed by every lane or by none
+    // ---- epilogue: out = O / l, lse = ln(sum of exp).  n_tiles is the same
+    // for the whole CTA, so the collective loads run on every lane or none.
     const bool have = n_tiles > 0;
-    if (have && ok && (*abort_flag || !mbar_wait(o_done, (uint32_t)(n_tiles - 1) & 1))) ok = false;
+    if (have && ok && (*abort_flag || !mbar_wait(o_final + G, 0))) ok = false;
     if (have) tc_fence_after();
     float* orow = p.out + (((size_t)b * p.Hq + h) * p.n_q + qi) * kD;
     const float inv = l > 0.f && ok ? 1.f / l : 0.f;
@@ -431,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c4 = 0; c4 < kD / 32; ++c4) {
       float o[32];
       if (have) {
-        tmem_ld32(trow + 128 + (uint32_t)c4 * 32, o);
+        tmem_ld32(tbase + 128 + (uint32_t)c4 * 32, o);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = 0.f;
@@ -471,7 +524,8 @@ cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const P
     if (e != cudaSuccess) return e;
     configured = dev;
   }
-  const dim3 grid((unsigned)((p.n_q + kM - 1) / kM), (unsigned)p.Hq, (unsigned)p.B);
+  const int groups = p.g % 2 == 0 ? 2 : 1;  // query heads per CTA
+  const dim3 grid((unsigned)((p.n_q + kM - 1) / kM), (unsigned)(p.Hq / groups), (unsigned)p.B);
   fd_prefill_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(tk, tv, p);
   return cudaGetLastError();
 }

@@ -137,3 +137,18 @@ def test_attend_dispatch(n_q, hq, hkv, dtype, expect):
     ref_out, ref_lse = oracle_rows(case, q, True)
     assert_close(np64(out), ref_out, "out")
     assert_close(np64(lse), ref_lse, "lse")
+
+
+def test_prefill_repeats_bit_identically():
+    """The same call twenty times gives the same bits (a pipeline race would show up as drift)."""
+    spec = small_spec("repeat", 2, 8, 2, 128, 700, lengths="uniform:1:700", q_gain=3.0)
+    case = make_case(spec, "cuda")
+    q = window_q(case, 200, seed=6)
+    first = run_prefill(case, q, True)
+    ref_out, ref_lse = oracle_rows(case, q, True)
+    torch.cuda.synchronize()
+    assert_close(np64(first[0]), ref_out, "out")
+    for _ in range(20):
+        o, l = run_prefill(case, q, True)
+        torch.cuda.synchronize()
+        assert torch.equal(o, first[0]) and torch.equal(l, first[1])
