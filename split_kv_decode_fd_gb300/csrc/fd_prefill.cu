@@ -148,6 +148,13 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[3
       : "memory");
 }
 
+// 2^x on the special-function unit (inputs here are <= 0 or -inf).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // x = hi + lo in bf16, packed as a pair (x0's part in the low half).
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
@@ -364,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // q row, times scale*log2(e), as bf16 hi / lo in the swizzled A layout
     {
       const float* qrow = p.q + (((size_t)b * p.Hq + h) * p.n_q + (qi < p.n_q ? qi : 0)) * kD;
-#pragma unroll 4
+#pragma unroll 8
       for (int c = 0; c < kD / 8; ++c) {
         float x[8];
         if (qi < p.n_q) {
@@ -404,27 +411,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c) s[32 + c] = a[c];
       }
-      float mx = -INFINITY;
+      // mask the keys past this row's limit (only the tiles that reach it)
+      const int32_t keys_left = lim - j * kN;
+      if (keys_left < kN) {
 #pragma unroll
-      for (int c = 0; c < kN; ++c) {
-        s[c] = j * kN + c < lim ? s[c] : -INFINITY;
-        mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < kN; ++c) s[c] = c < keys_left ? s[c] : -INFINITY;
       }
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < kN; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const bool rescale = mx > mref + kTau;
       float alpha = 1.f;
       if (rescale) {
         const float mn = fmaxf(mref, mx);
-        alpha = mref == -INFINITY ? 0.f : exp2f(mref - mn);
+        alpha = mref == -INFINITY ? 0.f : ex2(mref - mn);
         mref = mn;
       }
       const float base = mref == -INFINITY ? 0.f : mref;
-      float sum = 0.f;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < kN; ++c) {
-        s[c] = exp2f(s[c] - base);
-        sum += s[c];
+        s[c] = ex2(s[c] - base);
+        sum4[c & 3] += s[c];
       }
-      l = l * alpha + sum;
+      l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       // Rescaling O needs the previous tile's P.V to have finished.  tcgen05.ld
       // and st are warp-collective (.sync.aligned): the whole warp rescales
       // when any of its rows must, the others with alpha = 1.  P.V of tile j-1
