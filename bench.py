@@ -14,6 +14,7 @@ method has) on the host cores, on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import dataclasses
 import glob
 import hashlib
@@ -45,6 +46,8 @@ def parse_args():
                     help="run the workload with this batch size instead of its own (smaller profiling captures)")
     ap.add_argument("--append", action="store_true",
                     help="fused append-KV + decode (fd_append_decode): each step writes the last token's k/v")
+    ap.add_argument("--unfused", type=int, default=0, metavar="S",
+                    help="time fd_split_partial with S splits + fd_combine (two launches per step)")
     ap.add_argument("--rows", type=int, default=1,
                     help="query rows per sequence (causal window through fd_decode_rows); 1 = fd_decode")
     ap.add_argument("--no-graph", action="store_true",
@@ -347,6 +350,22 @@ def run_fdecode(args):
             fd.decode_rows(q_rows, case.k, case.v, causal=True, seq_lens=case.seq_lens,
                            max_seq_len=case.max_seq_len, block_table=case.block_table, scale=spec.scale,
                            n_splits=spec.n_splits, out=out, lse=lse, workspace=ws)
+    elif args.unfused:
+        spec = dataclasses.replace(spec, name=f"{spec.name}_unfused{args.unfused}")
+        o_part = torch.empty((spec.B, spec.Hq, args.unfused, spec.D), dtype=torch.float32, device=device)
+        m_part = torch.empty((spec.B, spec.Hq, args.unfused), dtype=torch.float32, device=device)
+        l_part = torch.empty_like(m_part)
+        lib = fd.load_library()
+        kvd = fd.fdecode._kv_desc(case.k, case.v, case.block_table)
+
+        def step():
+            s_ = torch.cuda.current_stream(device).cuda_stream
+            lib.fd_split_partial(case.q.data_ptr(), ctypes.byref(kvd), spec.B, spec.Hq, spec.Hkv,
+                                 case.seq_lens.data_ptr() if case.seq_lens is not None else None,
+                                 case.max_seq_len, spec.D, float(spec.scale), args.unfused, o_part.data_ptr(),
+                                 m_part.data_ptr(), l_part.data_ptr(), s_)
+            lib.fd_combine(o_part.data_ptr(), m_part.data_ptr(), l_part.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                           spec.B, spec.Hq, spec.D, args.unfused, s_)
     elif args.append:
         # the sequences' last token is the one appended: lengths before the append are L_b - 1
         lens_full = torch.tensor(case.lengths, dtype=torch.int32, device=device)
@@ -429,7 +448,7 @@ def run_fdecode(args):
     out_h = torch.empty(rows_shape + (spec.D,), dtype=torch.float32, pin_memory=True)
     lse_h = torch.empty(rows_shape, dtype=torch.float32, pin_memory=True)
     ws_h = fd.Workspace()
-    e2e_api = "fd_decode_host"
+    e2e_api = "fd_decode_host" if not args.unfused else "fd_decode_host (the fused path: the split + combine pair has no host-buffer entry)"
     if args.append:
         e2e_api = "pinned copies + fd_append_decode"
         q_dev = torch.empty_like(case.q)
@@ -486,7 +505,7 @@ def run_fdecode(args):
         return 0
     # ---- CPU baseline: the oracle on a bounded sample, host cores, rank 0 at N=1
     cpu = None
-    if world == 1 and not args.no_cpu_baseline and n_q == 1 and not args.append:
+    if world == 1 and not args.no_cpu_baseline and n_q == 1 and not args.append and not args.unfused:
         v, note, el = OracleSampler(case).whole_groups(args.cpu_seconds)
         cpu = {"value": v, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle", "sample": note,
                "seconds": round(el, 2)}
@@ -518,7 +537,7 @@ def run_fdecode(args):
                      "mean_launch_us": mean_launch_us},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": k_e2e, "api": e2e_api},
-        "gpu_launches": K,
+        "gpu_launches": K * (2 if args.unfused else 1),
         "clocks": clocks,
         "cpu_baseline": cpu,
         "kernel_status": gpd,

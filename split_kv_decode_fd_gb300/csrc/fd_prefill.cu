@@ -179,6 +179,34 @@ __device__ __forceinline__ int32_t row_keys(const PrefillParams& p, int32_t L, i
   return lim < 0 ? 0 : (lim > L ? L : lim);
 }
 
+// One work item: a tile of kM query rows of one sequence for `ngroups` heads.
+struct Item {
+  int32_t b, h0, m0, kvh, L, n_tiles;
+};
+
+// Items in order of decreasing work (causal: the latest query rows first), so
+// that the persistent CTAs, taking items round-robin, end close together.
+__device__ __forceinline__ Item item_of(const PrefillParams& p, int32_t idx, int32_t ngroups, int32_t n_m) {
+  const int32_t hp = p.Hq / ngroups;
+  const int32_t per_m = hp * p.B;
+  const int32_t mi = idx / per_m, rest = idx % per_m;
+  Item it;
+  it.m0 = (n_m - 1 - mi) * kM;
+  it.h0 = (rest % hp) * ngroups;
+  it.b = rest / hp;
+  it.kvh = it.h0 / p.g;
+  int32_t L = p.seq_lens ? __ldg(p.seq_lens + it.b) : p.max_len;
+  it.L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
+  const int32_t last_row = (p.n_q - it.m0 < kM ? p.n_q - it.m0 : kM) - 1;
+  const int32_t keys_max = row_keys(p, it.L, it.m0 + last_row);  // rows' limits grow with the row
+  it.n_tiles = (keys_max + kN - 1) / kN;
+  return it;
+}
+
+// Each CTA walks items blockIdx.x, + gridDim.x, ... (one item when launched
+// with a CTA per item).  Every role walks the same items, and all barrier
+// phases follow two running counters of the CTA: g, the key tiles processed so
+// far, and f, the items with at least one tile so far.
 __global__ void __launch_bounds__(kThreads, 1)
     fd_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                       const PrefillParams p) {
@@ -190,30 +218,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bars;        // [2 stages]
   uint64_t* kv_empty = bars + 2;   // [2 stages]
   // Every barrier a waiter might fall behind on alternates between two
-  // instances (tile j uses instance j % 2, phase j / 2), so that no barrier can
-  // complete two phases ahead of a parity wait: S of tile j+1 is issued before
-  // the MMA thread waits for P of tile j, so a fast softmax group may finish
-  // tiles j and j+1 meanwhile.
+  // instances (tile g uses instance g % 2, phase g / 2), so that no barrier can
+  // complete two phases ahead of a parity wait: S of tile g+1 is issued before
+  // the MMA thread waits for P of tile g, so a fast softmax group may finish
+  // tiles g and g+1 meanwhile.
   uint64_t* s_full = bars + 4;     // [2 groups][2]
   uint64_t* p_full = bars + 8;     // [2 groups][2]
   uint64_t* o_done = bars + 12;    // [2 groups][2]
-  uint64_t* o_final = bars + 16;   // [2 groups]: the group's last P.V has completed (one phase)
-  uint64_t* q_ready = bars + 18;
+  uint64_t* o_final = bars + 16;   // [2 groups]: an item's last P.V has completed
+  uint64_t* q_ready = bars + 18;   // an item's q tiles are in shared memory
   uint64_t* drain = bars + 19;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 160);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 164);
 
-  // Two query heads of one GQA group share the CTA (and every K/V tile) when
+  // Two query heads of one GQA group share an item (and every K/V tile) when
   // the group size is even; otherwise the second softmax group idles.
   const int32_t ngroups = (p.g % 2 == 0) ? 2 : 1;
-  const int32_t b = blockIdx.z, h0 = blockIdx.y * ngroups;
-  const int32_t m0 = (int32_t)(gridDim.x - 1 - blockIdx.x) * kM;  // longest causal tiles first
-  const int32_t kvh = h0 / p.g;
-  int32_t L = p.seq_lens ? __ldg(p.seq_lens + b) : p.max_len;
-  L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
-  const int32_t last_row = (p.n_q - m0 < kM ? p.n_q - m0 : kM) - 1;
-  const int32_t keys_max = row_keys(p, L, m0 + last_row);  // rows' limits grow with the row
-  const int32_t n_tiles = (keys_max + kN - 1) / kN;
+  const int32_t n_m = (p.n_q + kM - 1) / kM;
+  const int32_t n_items = n_m * (p.Hq / ngroups) * p.B;
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -249,105 +271,119 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int32_t issued = 0;
-    for (int32_t j = 0; j < n_tiles && ok; ++j) {
-      const uint32_t stage = j & 1, use = (uint32_t)j >> 1;
-      if (lane == 0 && (*abort_flag || !mbar_wait(kv_empty + stage, (use & 1) ^ 1))) ok = false;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      const int32_t t0 = j * kN;
-      const int32_t nvalid = L - t0 < kN ? L - t0 : kN;
-      const int32_t tok = t0 + 16 * lane;
-      bool mine = 16 * lane < nvalid;
-      int32_t row = tok, z = b * p.Hkv + kvh;
-      if (p.paged && mine) {
-        const int32_t page = __ldg(p.block_table + (size_t)b * p.max_pages + tok / p.page_size);
-        if (page < 0 || page >= p.num_pages) {
-          atomicOr(p.err, kErrBadIndex);
-          mine = false;
+    uint32_t g = 0;
+    for (int32_t idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+      const Item it = item_of(p, idx, ngroups, n_m);
+      for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
+        const uint32_t stage = g & 1, use = g >> 1;
+        if (lane == 0 && (*abort_flag || !mbar_wait(kv_empty + stage, (use & 1) ^ 1))) ok = false;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const int32_t t0 = j * kN;
+        const int32_t nvalid = it.L - t0 < kN ? it.L - t0 : kN;
+        const int32_t tok = t0 + 16 * lane;
+        bool mine = 16 * lane < nvalid;
+        int32_t row = tok, z = it.b * p.Hkv + it.kvh;
+        if (p.paged && mine) {
+          const int32_t page = __ldg(p.block_table + (size_t)it.b * p.max_pages + tok / p.page_size);
+          if (page < 0 || page >= p.num_pages) {
+            atomicOr(p.err, kErrBadIndex);
+            mine = false;
+          }
+          row = tok % p.page_size;
+          z = page * p.Hkv + it.kvh;
         }
-        row = tok % p.page_size;
-        z = page * p.Hkv + kvh;
-      }
-      const unsigned issue = __ballot_sync(0xffffffffu, mine);
-      if (lane == 0) mbar_arrive_expect_tx(kv_full + stage, (uint32_t)__popc(issue) * 4u * 2048u);
-      __syncwarp();
-      if (mine) {
-        uint8_t* kdst = smem + kStage0 + stage * kStageBytes + lane * 2048;
-        uint8_t* vdst = kdst + kTileBytes;
+        const unsigned issue = __ballot_sync(0xffffffffu, mine);
+        if (lane == 0) mbar_arrive_expect_tx(kv_full + stage, (uint32_t)__popc(issue) * 4u * 2048u);
+        __syncwarp();
+        if (mine) {
+          uint8_t* kdst = smem + kStage0 + stage * kStageBytes + lane * 2048;
+          uint8_t* vdst = kdst + kTileBytes;
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          tma_load_3d(kdst + blk * 8192, &tmap_k, kv_full + stage, blk * 64, row, z);
-          tma_load_3d(vdst + blk * 8192, &tmap_v, kv_full + stage, blk * 64, row, z);
+          for (int blk = 0; blk < 2; ++blk) {
+            tma_load_3d(kdst + blk * 8192, &tmap_k, kv_full + stage, blk * 64, row, z);
+            tma_load_3d(vdst + blk * 8192, &tmap_v, kv_full + stage, blk * 64, row, z);
+          }
         }
+        ++g;
       }
-      issued = j + 1;
     }
     if (!ok) *abort_flag = 1;
     // do not leave while this warp's copies may still be landing
     if (lane == 0) {
-      const int32_t first = issued > 2 ? issued - 2 : 0;
-      for (int32_t j = first; j < issued; ++j)
-        if (!mbar_wait(kv_full + (j & 1), ((uint32_t)j >> 1) & 1)) atomicOr(p.err, kErrTimeout);
+      const uint32_t first = g > 2 ? g - 2 : 0;
+      for (uint32_t t = first; t < g; ++t)
+        if (!mbar_wait(kv_full + (t & 1), (t >> 1) & 1)) atomicOr(p.err, kErrTimeout);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0) {
       constexpr uint32_t idS = instr_desc(kM, kN, false);
       constexpr uint32_t idO = instr_desc(kM, kD, true);
-      if (!mbar_wait(q_ready, 0)) ok = false;
-      tc_fence_after();
-      for (int32_t j = 0; j <= n_tiles && ok; ++j) {
-        if (j < n_tiles) {
-          const uint32_t stage = j & 1;
-          if (*abort_flag || !mbar_wait(kv_full + stage, ((uint32_t)j >> 1) & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t kt = sbase + kStage0 + stage * kStageBytes;
-          for (int G = 0; G < ngroups; ++G) {
-            const uint32_t d = tmem + (uint32_t)G * 256u + (uint32_t)(j & 1) * kN;
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-              const uint32_t qt = sbase + (uint32_t)G * kQGroupBytes + (part ? kQlo : kQhi);
-#pragma unroll
-              for (int s8 = 0; s8 < kD / 16; ++s8) {
-                const uint32_t off = (uint32_t)(s8 >> 2) * 8192u + (uint32_t)(s8 & 3) * 32u;
-                const uint64_t a = smem_desc(qt + (uint32_t)(s8 >> 2) * 16384u + (uint32_t)(s8 & 3) * 32u, 0, 1024);
-                const uint64_t bd = smem_desc(kt + off, 0, 1024);
-                umma(d, a, bd, idS, (part | s8) != 0);
-              }
-            }
-            umma_commit(s_full + G * 2 + (j & 1));
-          }
+      uint32_t g = 0, f = 0;
+      for (int32_t idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const Item it = item_of(p, idx, ngroups, n_m);
+        const int32_t n = it.n_tiles;
+        if (n == 0) continue;  // no q_ready phase either: the softmax skips such items too
+        if (*abort_flag || !mbar_wait(q_ready, f & 1)) {
+          ok = false;
+          break;
         }
-        if (j >= 1) {
-          const int32_t jj = j - 1;
-          const uint32_t stage = jj & 1;
-          const uint32_t vt = sbase + kStage0 + stage * kStageBytes + kTileBytes;
-          for (int G = 0; G < ngroups && ok; ++G) {
-            if (*abort_flag || !mbar_wait(p_full + G * 2 + (jj & 1), ((uint32_t)jj >> 1) & 1)) {
+        tc_fence_after();
+        for (int32_t j = 0; j <= n && ok; ++j) {
+          if (j < n) {
+            const uint32_t gj = g + j, stage = gj & 1;
+            if (*abort_flag || !mbar_wait(kv_full + stage, (gj >> 1) & 1)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t pt = tmem + (uint32_t)G * 256u + (uint32_t)(jj & 1) * kN;  // P hi [0, 32), lo [32, 64)
+            const uint32_t kt = sbase + kStage0 + stage * kStageBytes;
+            for (int G = 0; G < ngroups; ++G) {
+              const uint32_t d = tmem + (uint32_t)G * 256u + (gj & 1) * kN;
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
+              for (int part = 0; part < 2; ++part) {
+                const uint32_t qt = sbase + (uint32_t)G * kQGroupBytes + (part ? kQlo : kQhi);
 #pragma unroll
-              for (int kk = 0; kk < kN / 16; ++kk) {
-                const uint64_t bd = smem_desc(vt + (uint32_t)kk * 2048u, 8192, 1024);
-                umma_tmem_a(tmem + (uint32_t)G * 256u + 128u, pt + (uint32_t)part * (kN / 2) + (uint32_t)kk * 8u, bd,
-                            idO, (jj | part | kk) != 0);
+                for (int s8 = 0; s8 < kD / 16; ++s8) {
+                  const uint32_t off = (uint32_t)(s8 >> 2) * 8192u + (uint32_t)(s8 & 3) * 32u;
+                  const uint64_t a =
+                      smem_desc(qt + (uint32_t)(s8 >> 2) * 16384u + (uint32_t)(s8 & 3) * 32u, 0, 1024);
+                  const uint64_t bd = smem_desc(kt + off, 0, 1024);
+                  umma(d, a, bd, idS, (part | s8) != 0);
+                }
               }
+              umma_commit(s_full + G * 2 + (gj & 1));
             }
-            umma_commit(o_done + G * 2 + (jj & 1));
-            if (jj == n_tiles - 1) umma_commit(o_final + G);
           }
-          if (!ok) break;
-          umma_commit(kv_empty + stage);
+          if (j >= 1) {
+            const uint32_t gj = g + j - 1, stage = gj & 1;
+            const uint32_t vt = sbase + kStage0 + stage * kStageBytes + kTileBytes;
+            for (int G = 0; G < ngroups && ok; ++G) {
+              if (*abort_flag || !mbar_wait(p_full + G * 2 + (gj & 1), (gj >> 1) & 1)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t pt = tmem + (uint32_t)G * 256u + (gj & 1) * kN;  // P hi [0, 32), lo [32, 64)
+#pragma unroll
+              for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                for (int kk = 0; kk < kN / 16; ++kk) {
+                  const uint64_t bd = smem_desc(vt + (uint32_t)kk * 2048u, 8192, 1024);
+                  umma_tmem_a(tmem + (uint32_t)G * 256u + 128u, pt + (uint32_t)part * (kN / 2) + (uint32_t)kk * 8u,
+                              bd, idO, ((j - 1) | part | kk) != 0);
+                }
+              }
+              umma_commit(o_done + G * 2 + (gj & 1));
+              if (j == n) umma_commit(o_final + G);
+            }
+            if (!ok) break;
+            umma_commit(kv_empty + stage);
+          }
         }
+        g += n;
+        ++f;
       }
       if (!ok) {
         *abort_flag = 1;
@@ -360,155 +396,167 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if ((warp - 2) / 4 < ngroups) {
     // ------------------------------------------------------------ softmax, group G
     const int32_t G = (warp - 2) / 4;
-    const int32_t h = h0 + G;
     const int32_t quarter = warp & 3;
     const int32_t r = quarter * 32 + lane;  // query row in the tile = TMEM lane
-    const int32_t qi = m0 + r;
-    const int32_t lim = row_keys(p, L, qi);
     const uint32_t tbase = tmem + (uint32_t)G * 256u + ((uint32_t)(quarter * 32) << 16);
     const uint32_t qbase = sbase + (uint32_t)G * kQGroupBytes;
     uint64_t* my_s_full = s_full + G * 2;
-    // q row, times scale*log2(e), as bf16 hi / lo in the swizzled A layout
-    {
-      const float* qrow = p.q + (((size_t)b * p.Hq + h) * p.n_q + (qi < p.n_q ? qi : 0)) * kD;
+    uint32_t g = 0, f = 0;
+    for (int32_t idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
+      const Item it = item_of(p, idx, ngroups, n_m);
+      const int32_t n = it.n_tiles;
+      const int32_t h = it.h0 + G;
+      const int32_t qi = it.m0 + r;
+      const int32_t lim = row_keys(p, it.L, qi);
+      if (n > 0) {
+        // q row, times scale*log2(e), as bf16 hi / lo in the swizzled A layout.  The
+        // previous item's MMAs are all complete (its epilogue waited o_final).
+        const float* qrow = p.q + (((size_t)it.b * p.Hq + h) * p.n_q + (qi < p.n_q ? qi : 0)) * kD;
 #pragma unroll 8
-      for (int c = 0; c < kD / 8; ++c) {
-        float x[8];
-        if (qi < p.n_q) {
-          const float4 a0 = __ldg(reinterpret_cast<const float4*>(qrow) + 2 * c);
-          const float4 a1 = __ldg(reinterpret_cast<const float4*>(qrow) + 2 * c + 1);
-          x[0] = a0.x; x[1] = a0.y; x[2] = a0.z; x[3] = a0.w;
-          x[4] = a1.x; x[5] = a1.y; x[6] = a1.z; x[7] = a1.w;
+        for (int c = 0; c < kD / 8; ++c) {
+          float x[8];
+          if (qi < p.n_q) {
+            const float4 a0 = __ldg(reinterpret_cast<const float4*>(qrow) + 2 * c);
+            const float4 a1 = __ldg(reinterpret_cast<const float4*>(qrow) + 2 * c + 1);
+            x[0] = a0.x; x[1] = a0.y; x[2] = a0.z; x[3] = a0.w;
+            x[4] = a1.x; x[5] = a1.y; x[6] = a1.z; x[7] = a1.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+          }
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split2(x[2 * e] * p.qk_scale, x[2 * e + 1] * p.qk_scale, hi[e], lo[e]);
+          const uint32_t off = (uint32_t)(c >> 3) * 16384u + swz((uint32_t)r, (uint32_t)(c & 7));
+          sts128(qbase + kQhi + off, hi[0], hi[1], hi[2], hi[3]);
+          sts128(qbase + kQlo + off, lo[0], lo[1], lo[2], lo[3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_ready);
+      }
+
+      // A failed wait never leaves the loop early (the named barrier below needs
+      // all 128 threads of the group): later waits are skipped, the output flagged.
+      float mref = -INFINITY, l = 0.f;
+      for (int32_t j = 0; j < n; ++j) {
+        const uint32_t gj = g + j;
+        if (ok && (*abort_flag || !mbar_wait(my_s_full + (gj & 1), (gj >> 1) & 1))) ok = false;
+        tc_fence_after();
+        float s[kN];
+        {
+          float a[32];
+          tmem_ld32(tbase + (gj & 1) * kN, a);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[c] = a[c];
+          tmem_ld32(tbase + (gj & 1) * kN + 32, a);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[32 + c] = a[c];
+        }
+        // mask the keys past this row's limit (only the tiles that reach it)
+        const int32_t keys_left = lim - j * kN;
+        if (keys_left < kN) {
+#pragma unroll
+          for (int c = 0; c < kN; ++c) s[c] = c < keys_left ? s[c] : -INFINITY;
+        }
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < kN; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        const bool rescale = mx > mref + kTau;
+        float alpha = 1.f;
+        if (rescale) {
+          const float mn = fmaxf(mref, mx);
+          alpha = mref == -INFINITY ? 0.f : ex2(mref - mn);
+          mref = mn;
+        }
+        const float base = mref == -INFINITY ? 0.f : mref;
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < kN; ++c) {
+          s[c] = ex2(s[c] - base);
+          sum4[c & 3] += s[c];
+        }
+        l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+        // Rescaling O needs the previous tile's P.V to have finished.  tcgen05.ld
+        // and st are warp-collective (.sync.aligned): the whole warp rescales
+        // when any of its rows must, the others with alpha = 1.  P.V of tile g-1
+        // completes phase (g-1)/2 of o_done[G][(g-1)%2]; a parity wait for it is
+        // exact although earlier phases were not waited: that barrier's previous
+        // phase (tile g-3) finished before this tile's S (issued after it, in
+        // order), and its next one (tile g+1) needs this group's P first.
+        if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+          if (ok && (*abort_flag || !mbar_wait(o_done + G * 2 + ((gj - 1) & 1), ((gj - 1) >> 1) & 1))) ok = false;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c4 = 0; c4 < kD / 32; ++c4) {
+            float o[32];
+            tmem_ld32(tbase + 128 + (uint32_t)c4 * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tbase + 128 + (uint32_t)c4 * 32, o);
+          }
+        }
+        if (G == 0 && j == n - 1 && it.L - j * kN < kN) {
+          // keys past L in the last tile get p = 0, but 0 * NaN is NaN: zero those V
+          // rows (group 0 does it for both: its P.V is issued first)
+          const uint32_t stage = gj & 1;
+          if (ok && (*abort_flag || !mbar_wait(kv_full + stage, (gj >> 1) & 1))) ok = false;
+          const int32_t nvalid = it.L - j * kN;
+          const uint32_t vt = sbase + kStage0 + stage * kStageBytes + kTileBytes;
+          const int32_t tid2 = (warp - 2) * 32 + lane;
+          for (int32_t e = tid2; e < (kN - nvalid) * 16; e += 128) {
+            const uint32_t row = (uint32_t)(nvalid + e / 16), c = (uint32_t)(e % 16);
+            sts128(vt + (c >> 3) * 8192u + row * 128u + ((c & 7u) << 4), 0u, 0u, 0u, 0u);
+          }
+        }
+        // P over this tile's S columns: hi in [0, 32), lo in [32, 64), two keys per column
+        {
+          uint32_t hi[32], lo[32];
+#pragma unroll
+          for (int c = 0; c < kN / 2; ++c) split2(s[2 * c], s[2 * c + 1], hi[c], lo[c]);
+          const uint32_t pt = tbase + (gj & 1) * kN;
+          tmem_st32u(pt, hi);
+          tmem_st32u(pt + kN / 2, lo);
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the zeroed V rows, if any
+        tc_fence_before();
+        named_barrier(1 + G, 128);  // every thread of the group has stored before the arrival
+        if (lane == 0) mbar_arrive(p_full + G * 2 + (gj & 1));
+      }
+      // ---- epilogue: out = O / l, lse = ln(sum of exp).  n is the same for the
+      // whole CTA, so the collective loads run on every lane or none.
+      if (n > 0) {
+        if (ok && (*abort_flag || !mbar_wait(o_final + G, f & 1))) ok = false;
+        tc_fence_after();
+      }
+      float* orow = p.out + (((size_t)it.b * p.Hq + h) * p.n_q + qi) * kD;
+      const float inv = l > 0.f && ok ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int c4 = 0; c4 < kD / 32; ++c4) {
+        float o[32];
+        if (n > 0) {
+          tmem_ld32(tbase + 128 + (uint32_t)c4 * 32, o);
         } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+          for (int i = 0; i < 32; ++i) o[i] = 0.f;
         }
-        uint32_t hi[4], lo[4];
+        if (qi < p.n_q) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) split2(x[2 * e] * p.qk_scale, x[2 * e + 1] * p.qk_scale, hi[e], lo[e]);
-        const uint32_t off = (uint32_t)(c >> 3) * 16384u + swz((uint32_t)r, (uint32_t)(c & 7));
-        sts128(qbase + kQhi + off, hi[0], hi[1], hi[2], hi[3]);
-        sts128(qbase + kQlo + off, lo[0], lo[1], lo[2], lo[3]);
-      }
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncwarp();
-    if (lane == 0) mbar_arrive(q_ready);
-
-    // A failed wait never leaves the loop early (the named barrier below needs
-    // all 128 threads of the group): later waits are skipped, the output flagged.
-    float mref = -INFINITY, l = 0.f;
-    for (int32_t j = 0; j < n_tiles; ++j) {
-      if (ok && (*abort_flag || !mbar_wait(my_s_full + (j & 1), ((uint32_t)j >> 1) & 1))) ok = false;
-      tc_fence_after();
-      float s[kN];
-      {
-        float a[32];
-        tmem_ld32(tbase + (uint32_t)(j & 1) * kN, a);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) s[c] = a[c];
-        tmem_ld32(tbase + (uint32_t)(j & 1) * kN + 32, a);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) s[32 + c] = a[c];
-      }
-      // mask the keys past this row's limit (only the tiles that reach it)
-      const int32_t keys_left = lim - j * kN;
-      if (keys_left < kN) {
-#pragma unroll
-        for (int c = 0; c < kN; ++c) s[c] = c < keys_left ? s[c] : -INFINITY;
-      }
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < kN; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      const bool rescale = mx > mref + kTau;
-      float alpha = 1.f;
-      if (rescale) {
-        const float mn = fmaxf(mref, mx);
-        alpha = mref == -INFINITY ? 0.f : ex2(mref - mn);
-        mref = mn;
-      }
-      const float base = mref == -INFINITY ? 0.f : mref;
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < kN; ++c) {
-        s[c] = ex2(s[c] - base);
-        sum4[c & 3] += s[c];
-      }
-      l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-      // Rescaling O needs the previous tile's P.V to have finished.  tcgen05.ld
-      // and st are warp-collective (.sync.aligned): the whole warp rescales
-      // when any of its rows must, the others with alpha = 1.  P.V of tile j-1
-      // completes phase (j-1)/2 of o_done[G][(j-1)%2]; a parity wait for it is
-      // exact although earlier phases were not waited: that barrier's previous
-      // phase (tile j-3) finished before this tile's S (issued after it, in
-      // order), and its next one (tile j+1) needs this group's P first.
-      if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
-        if (ok && (*abort_flag || !mbar_wait(o_done + G * 2 + ((j - 1) & 1), ((uint32_t)(j - 1) >> 1) & 1)))
-          ok = false;
-        tc_fence_after();
-#pragma unroll 1
-        for (int c4 = 0; c4 < kD / 32; ++c4) {
-          float o[32];
-          tmem_ld32(tbase + 128 + (uint32_t)c4 * 32, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(tbase + 128 + (uint32_t)c4 * 32, o);
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(orow + c4 * 32 + i) =
+                make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
         }
       }
-      if (G == 0 && j == n_tiles - 1 && L - j * kN < kN) {
-        // keys past L in the last tile get p = 0, but 0 * NaN is NaN: zero those V
-        // rows (group 0 does it for both: its P.V is issued first)
-        const uint32_t stage = j & 1;
-        if (ok && (*abort_flag || !mbar_wait(kv_full + stage, ((uint32_t)j >> 1) & 1))) ok = false;
-        const int32_t nvalid = L - j * kN;
-        const uint32_t vt = sbase + kStage0 + stage * kStageBytes + kTileBytes;
-        const int32_t tid2 = (warp - 2) * 32 + lane;
-        for (int32_t idx = tid2; idx < (kN - nvalid) * 16; idx += 128) {
-          const uint32_t row = (uint32_t)(nvalid + idx / 16), c = (uint32_t)(idx % 16);
-          sts128(vt + (c >> 3) * 8192u + row * 128u + ((c & 7u) << 4), 0u, 0u, 0u, 0u);
-        }
-      }
-      // P over this tile's S columns: hi in [0, 32), lo in [32, 64), two keys per column
-      {
-        uint32_t hi[32], lo[32];
-#pragma unroll
-        for (int c = 0; c < kN / 2; ++c) split2(s[2 * c], s[2 * c + 1], hi[c], lo[c]);
-        const uint32_t pt = tbase + (uint32_t)(j & 1) * kN;
-        tmem_st32u(pt, hi);
-        tmem_st32u(pt + kN / 2, lo);
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the zeroed V rows, if any
+      if (qi < p.n_q && p.lse)
+        p.lse[((size_t)it.b * p.Hq + h) * p.n_q + qi] = l > 0.f ? (mref + log2f(l)) * kLn2f : -INFINITY;
+      // this group's O columns are read before the next item's first P.V (which
+      // needs this group's P) overwrites them
       tc_fence_before();
-      named_barrier(1 + G, 128);  // every thread of the group has stored before the arrival
-      if (lane == 0) mbar_arrive(p_full + G * 2 + (j & 1));
+      g += n;
+      if (n > 0) ++f;
     }
-    // ---- epilogue: out = O / l, lse = ln(sum of exp).  n_tiles is the same
-    // for the whole CTA, so the collective loads run on every lane or none.
-    const bool have = n_tiles > 0;
-    if (have && ok && (*abort_flag || !mbar_wait(o_final + G, 0))) ok = false;
-    if (have) tc_fence_after();
-    float* orow = p.out + (((size_t)b * p.Hq + h) * p.n_q + qi) * kD;
-    const float inv = l > 0.f && ok ? 1.f / l : 0.f;
-#pragma unroll 1
-    for (int c4 = 0; c4 < kD / 32; ++c4) {
-      float o[32];
-      if (have) {
-        tmem_ld32(tbase + 128 + (uint32_t)c4 * 32, o);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0.f;
-      }
-      if (qi < p.n_q) {
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(orow + c4 * 32 + i) =
-              make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
-      }
-    }
-    if (qi < p.n_q && p.lse)
-      p.lse[((size_t)b * p.Hq + h) * p.n_q + qi] = l > 0.f ? (mref + log2f(l)) * kLn2f : -INFINITY;
     if (!ok) {
       *abort_flag = 1;
       atomicOr(p.err, kErrTimeout);
@@ -535,8 +583,13 @@ cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const P
     if (e != cudaSuccess) return e;
     configured = dev;
   }
-  const int groups = p.g % 2 == 0 ? 2 : 1;  // query heads per CTA
-  const dim3 grid((unsigned)((p.n_q + kM - 1) / kM), (unsigned)(p.Hq / groups), (unsigned)p.B);
+  // One CTA per item, items numbered longest first: the hardware hands the next
+  // item to whichever SM frees up (measured faster than persistent CTAs taking
+  // items round-robin, whose tails do not even out).
+  const int groups = p.g % 2 == 0 ? 2 : 1;  // query heads per item
+  const int64_t items = (int64_t)((p.n_q + kM - 1) / kM) * (p.Hq / groups) * p.B;
+  if (items > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)items);
   fd_prefill_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(tk, tv, p);
   return cudaGetLastError();
 }
