@@ -253,3 +253,46 @@ def test_append_decode_rejects_bad_arguments(lib, case, expected):
                               ctypes.byref(kv), FAKE, None, 1, 4, 4, None, case.get("max_len", 1023), 128, 0.1, 4,
                               FAKE, case.get("ws_bytes", 1 << 30), None)
     assert st == expected
+
+
+def _prefill(lib, kv, n_q=100, causal=1, D=128, ws=FAKE, ws_bytes=4096, max_len=1024, q=FAKE):
+    return lib.fd_prefill(q, n_q, causal, ctypes.byref(kv), FAKE, None, 1, 4, 4, None, max_len, D, 0.1, ws,
+                          ws_bytes, None)
+
+
+@pytest.mark.parametrize("case,expected", [
+    (dict(n_q=0), fdb.FD_ERR_INVALID_ARG),
+    (dict(causal=3), fdb.FD_ERR_INVALID_ARG),
+    (dict(q=0), fdb.FD_ERR_INVALID_ARG),
+    (dict(ws=0), fdb.FD_ERR_INVALID_ARG),
+    (dict(ws_bytes=16), fdb.FD_ERR_WORKSPACE_TOO_SMALL),
+    (dict(D=64), fdb.FD_ERR_UNSUPPORTED),            # the query-tile kernel is built for D = 128
+    (dict(max_len=2048), fdb.FD_ERR_INVALID_ARG),    # longer than the cache
+])
+def test_prefill_rejects_bad_arguments(lib, case, expected):
+    assert _prefill(lib, _kv(), **case) == expected
+
+
+def test_prefill_needs_a_bf16_cache(lib):
+    assert _prefill(lib, _kv(dtype=fdb.FD_F32)) == fdb.FD_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("n_q,hq,hkv,d,dtype,expect", [
+    (1, 32, 8, 128, "bf16", "decode"),
+    (4, 32, 8, 128, "bf16", "decode_rows"),   # 4 rows x 4 heads per KV head = 16
+    (5, 32, 8, 128, "bf16", "prefill"),
+    (16, 4, 4, 128, "bf16", "decode_rows"),   # 16 rows x 1 head
+    (17, 4, 4, 128, "bf16", "prefill"),
+    (64, 4, 4, 64, "bf16", "decode_rows"),    # D = 64 has no query-tile kernel: rows up to 64
+    (64, 4, 4, 128, "f32", "decode_rows"),
+    (65, 4, 4, 128, "f32", "none"),
+])
+def test_phase_dispatch_choice(lib, n_q, hq, hkv, d, dtype, expect):
+    assert fd.attend_backend(n_q, hq, hkv, d, dtype).startswith(expect)
+
+
+def test_attend_reports_unsupported(lib):
+    chosen = ctypes.c_int32(7)
+    st = lib.fd_attend(FAKE, 65, 1, ctypes.byref(_kv(dtype=fdb.FD_F32)), FAKE, None, 1, 4, 4, None, 1024, 128, 0.1,
+                       0, FAKE, 1 << 20, None, ctypes.byref(chosen))
+    assert st == fdb.FD_ERR_UNSUPPORTED and chosen.value == -1
