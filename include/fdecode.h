@@ -207,7 +207,7 @@ FD_API fd_status fd_append_decode(const float* q, const void* k_new, const void*
  * accumulators) instead of rows-as-heads.  "FlashDecoding and split-KV",
  * section "Walking through it": prefill has many query rows and wants
  * FlashAttention's tiling along them; decode has one.
- *   Supports D = 128 with a bf16 cache (contiguous or paged); any n_q >= 1.
+ *   Supports D = 64 and 128 with a bf16 cache (contiguous or paged); any n_q >= 1.
  *   workspace: at least 256 bytes, zero-filled once (its first word is the
  *   kernels' error word, read by fd_workspace_status).  out, lse as in
  *   fd_decode_rows.  One launch, asynchronous on `stream`.
@@ -224,7 +224,7 @@ FD_API fd_status fd_prefill(const float* q, int32_t n_q, int32_t causal, const f
  *   FD_BACKEND_DECODE       n_q == 1                      -> fd_decode
  *   FD_BACKEND_DECODE_ROWS  n_q * (Hq / Hkv) <= 16, or no prefill kernel for
  *                           this D / dtype and n_q <= 64  -> fd_decode_rows
- *   FD_BACKEND_PREFILL      otherwise (D = 128, bf16)     -> fd_prefill
+ *   FD_BACKEND_PREFILL      otherwise (D = 64 or 128, bf16) -> fd_prefill
  * fd_attend_backend returns the choice without running anything (-1: no
  * backend); fd_backend_name names it.  The workspace must fit the chosen
  * backend: fd_workspace_bytes(B, Hq * n_q, Hkv, D, n_splits, 0) for the decode

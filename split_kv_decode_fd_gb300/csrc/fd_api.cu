@@ -432,7 +432,7 @@ fd_status fd_prefill(const float* q, int32_t n_q, int32_t causal, const fd_kv_de
   if (n_q < 1 || (causal != 0 && causal != 1)) return FD_ERR_INVALID_ARG;
   if (workspace_bytes < kHeaderBytes) return FD_ERR_WORKSPACE_TOO_SMALL;
   if ((st = check_kv(kv, B, Hkv, max_seq_len)) != FD_OK) return st;
-  if (D != 128 || kv->dtype != FD_BF16) return FD_ERR_UNSUPPORTED;
+  if (kv->dtype != FD_BF16) return FD_ERR_UNSUPPORTED;
   if (B > 65535 || Hq > 65535 || (int64_t)B * Hq * n_q * D > ((int64_t)1 << 40)) return FD_ERR_UNSUPPORTED;
   CUtensorMap tk, tv;
   if ((st = make_maps(kv, B, Hkv, D, &tk, &tv)) != FD_OK) return st;
@@ -456,13 +456,13 @@ fd_status fd_prefill(const float* q, int32_t n_q, int32_t causal, const fd_kv_de
   p.max_pages = kv->max_pages_per_seq;
   p.num_pages = kv->num_pages;
   p.qk_scale = (float)((double)scale * 1.4426950408889634);
-  return launch_prefill(tk, tv, p, (cudaStream_t)stream) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+  return launch_prefill(D, tk, tv, p, (cudaStream_t)stream) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
 int32_t fd_attend_backend(int32_t n_q, int32_t Hq, int32_t Hkv, int32_t D, int32_t kv_dtype) {
   if (n_q < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return -1;
   if (n_q == 1) return FD_BACKEND_DECODE;
-  const bool prefill_ok = D == 128 && kv_dtype == FD_BF16;
+  const bool prefill_ok = (D == 64 || D == 128) && kv_dtype == FD_BF16;
   if ((int64_t)n_q * (Hq / Hkv) <= kMaxGroupBf16 || (!prefill_ok && n_q <= 64)) return FD_BACKEND_DECODE_ROWS;
   return prefill_ok ? FD_BACKEND_PREFILL : -1;
 }

@@ -40,22 +40,28 @@ namespace {
 
 constexpr int kM = kPrefillRows;   // query rows per CTA (TMEM lanes)
 constexpr int kN = kPrefillKeys;   // keys per tile
-constexpr int kD = 128;            // head dim
 constexpr int kThreads = 320;      // producer, MMA, two softmax groups of four warps
 constexpr float kTau = 8.0f;
 constexpr float kLn2f = 0.6931471805599453f;
+constexpr uint32_t kTmemCols = 512;  // per group (256 each): S / P at +0 and +64, O (D columns) at +128
 
-// shared memory (byte offsets from a 1024-aligned base)
-constexpr uint32_t kQhi = 0;                  // per group: [2 col blocks][128 rows][128 B] bf16, hi then lo
-constexpr uint32_t kQlo = 32768;
-constexpr uint32_t kQGroupBytes = 65536;
-constexpr uint32_t kStage0 = 131072;          // per stage: K [2][64][128 B] then V [2][64][128 B]
-constexpr uint32_t kStageBytes = 32768;
-constexpr uint32_t kTileBytes = 16384;
-constexpr uint32_t kBarOff = 196608;
-constexpr uint32_t kSmemBytes = kBarOff + 256;
-constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
-constexpr uint32_t kTmemCols = 512;           // per group (256 each): S / P at +0 and +64, O at +128
+// Shared-memory layout for head dim D (64 or 128), byte offsets from a
+// 1024-aligned base.  A row of D bf16 is D/64 column blocks of 128 bytes.
+template <int D>
+struct PLayout {
+  static constexpr int kNB = D / 64;
+  static constexpr uint32_t kQhi = 0;                           // per group: [kNB][128 rows][128 B] hi, then lo
+  static constexpr uint32_t kQlo = kNB * 16384u;
+  static constexpr uint32_t kQGroupBytes = 2 * kQlo;
+  static constexpr uint32_t kTileBytes = kNB * 8192u;           // [kNB][64 rows][128 B]
+  static constexpr uint32_t kStageBytes = 2 * kTileBytes;       // K then V
+  static constexpr uint32_t kStage0 = 2 * kQGroupBytes;
+  static constexpr uint32_t kBarOff = kStage0 + 2 * kStageBytes;
+  // at least 116 KB, so that one CTA fits per SM: each allocates all 512 TMEM columns
+  static constexpr uint32_t kSmemNeed = kBarOff + 256 + 1024;
+  static constexpr uint32_t kSmemAlloc = kSmemNeed > 118784u ? kSmemNeed : 118784u;
+  static_assert(D == 64 || D == 128, "head dim");
+};
 
 // ---------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor (sm_100 family): start address, leading and
@@ -207,9 +213,16 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int32_t idx, int
 // with a CTA per item).  Every role walks the same items, and all barrier
 // phases follow two running counters of the CTA: g, the key tiles processed so
 // far, and f, the items with at least one tile so far.
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fd_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                       const PrefillParams p) {
+  using Lay = PLayout<D>;
+  constexpr int kD = D;
+  constexpr int kNB = Lay::kNB;
+  constexpr uint32_t kQhi = Lay::kQhi, kQlo = Lay::kQlo, kQGroupBytes = Lay::kQGroupBytes;
+  constexpr uint32_t kTileBytes = Lay::kTileBytes, kStageBytes = Lay::kStageBytes, kStage0 = Lay::kStage0;
+  constexpr uint32_t kBarOff = Lay::kBarOff;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
@@ -294,13 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           z = page * p.Hkv + it.kvh;
         }
         const unsigned issue = __ballot_sync(0xffffffffu, mine);
-        if (lane == 0) mbar_arrive_expect_tx(kv_full + stage, (uint32_t)__popc(issue) * 4u * 2048u);
+        if (lane == 0) mbar_arrive_expect_tx(kv_full + stage, (uint32_t)__popc(issue) * 2u * kNB * 2048u);
         __syncwarp();
         if (mine) {
           uint8_t* kdst = smem + kStage0 + stage * kStageBytes + lane * 2048;
           uint8_t* vdst = kdst + kTileBytes;
 #pragma unroll
-          for (int blk = 0; blk < 2; ++blk) {
+          for (int blk = 0; blk < kNB; ++blk) {
             tma_load_3d(kdst + blk * 8192, &tmap_k, kv_full + stage, blk * 64, row, z);
             tma_load_3d(vdst + blk * 8192, &tmap_v, kv_full + stage, blk * 64, row, z);
           }
@@ -505,8 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int32_t nvalid = it.L - j * kN;
           const uint32_t vt = sbase + kStage0 + stage * kStageBytes + kTileBytes;
           const int32_t tid2 = (warp - 2) * 32 + lane;
-          for (int32_t e = tid2; e < (kN - nvalid) * 16; e += 128) {
-            const uint32_t row = (uint32_t)(nvalid + e / 16), c = (uint32_t)(e % 16);
+          constexpr int kRowChunks = kD * 2 / 16;
+          for (int32_t e = tid2; e < (kN - nvalid) * kRowChunks; e += 128) {
+            const uint32_t row = (uint32_t)(nvalid + e / kRowChunks), c = (uint32_t)(e % kRowChunks);
             sts128(vt + (c >> 3) * 8192u + row * 128u + ((c & 7u) << 4), 0u, 0u, 0u, 0u);
           }
         }
@@ -570,16 +584,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-}  // namespace
-
-cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
-                           cudaStream_t stream) {
+template <int D>
+cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                             cudaStream_t stream) {
   static int configured = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured != dev) {
-    e = cudaFuncSetAttribute(fd_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+    e = cudaFuncSetAttribute(fd_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)PLayout<D>::kSmemAlloc);
     if (e != cudaSuccess) return e;
     configured = dev;
   }
@@ -590,8 +604,17 @@ cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const P
   const int64_t items = (int64_t)((p.n_q + kM - 1) / kM) * (p.Hq / groups) * p.B;
   if (items > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)items);
-  fd_prefill_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(tk, tv, p);
+  fd_prefill_kernel<D><<<grid, kThreads, PLayout<D>::kSmemAlloc, stream>>>(tk, tv, p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(int D, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                           cudaStream_t stream) {
+  if (D == 128) return launch_prefill_t<128>(tk, tv, p, stream);
+  if (D == 64) return launch_prefill_t<64>(tk, tv, p, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fdk

@@ -24,7 +24,8 @@ struct PrefillParams {
 constexpr int kPrefillRows = 128;
 constexpr int kPrefillKeys = 64;
 
-cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+// D = 64 or 128; cudaErrorInvalidValue otherwise.
+cudaError_t launch_prefill(int D, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                            cudaStream_t stream);
 
 }  // namespace fdk

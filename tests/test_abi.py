@@ -266,7 +266,7 @@ def _prefill(lib, kv, n_q=100, causal=1, D=128, ws=FAKE, ws_bytes=4096, max_len=
     (dict(q=0), fdb.FD_ERR_INVALID_ARG),
     (dict(ws=0), fdb.FD_ERR_INVALID_ARG),
     (dict(ws_bytes=16), fdb.FD_ERR_WORKSPACE_TOO_SMALL),
-    (dict(D=64), fdb.FD_ERR_UNSUPPORTED),            # the query-tile kernel is built for D = 128
+    (dict(D=96), fdb.FD_ERR_UNSUPPORTED),            # the query-tile kernel is built for D = 64 and 128
     (dict(max_len=2048), fdb.FD_ERR_INVALID_ARG),    # longer than the cache
 ])
 def test_prefill_rejects_bad_arguments(lib, case, expected):
@@ -283,7 +283,8 @@ def test_prefill_needs_a_bf16_cache(lib):
     (5, 32, 8, 128, "bf16", "prefill"),
     (16, 4, 4, 128, "bf16", "decode_rows"),   # 16 rows x 1 head
     (17, 4, 4, 128, "bf16", "prefill"),
-    (64, 4, 4, 64, "bf16", "decode_rows"),    # D = 64 has no query-tile kernel: rows up to 64
+    (64, 4, 4, 64, "bf16", "prefill"),
+    (64, 4, 4, 96, "bf16", "decode_rows"),    # no query-tile kernel for this D: rows up to 64
     (64, 4, 4, 128, "f32", "decode_rows"),
     (65, 4, 4, 128, "f32", "none"),
 ])

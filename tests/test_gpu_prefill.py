@@ -45,6 +45,8 @@ SPECS = [
     (small_spec("peaked", 1, 4, 1, 128, 520, q_gain=6.0), 260),
     (small_spec("paged16_gqa4", 3, 8, 2, 128, 600, layout="paged", page_size=16, lengths="uniform:1:600"), 150),
     (small_spec("paged64_mha", 2, 2, 2, 128, 500, layout="paged", page_size=64, lengths="uniform:200:500"), 64),
+    (small_spec("d64_gqa4", 2, 8, 2, 64, 600, lengths="uniform:1:600"), 300),
+    (small_spec("d64_paged32_mha", 2, 3, 3, 64, 400, layout="paged", page_size=32, lengths="uniform:100:400"), 150),
 ]
 
 
@@ -111,7 +113,8 @@ def test_prefill_long_prompt_sampled():
 
 
 def test_prefill_rejects_what_it_does_not_cover():
-    for spec in (small_spec("d64", 1, 2, 2, 64, 64), small_spec("f32", 1, 2, 2, 128, 64, kv_dtype="f32")):
+    for spec in (small_spec("f32", 1, 2, 2, 128, 64, kv_dtype="f32"), small_spec("f32d64", 1, 2, 2, 64, 64,
+                                                                                 kv_dtype="f32")):
         case = make_case(spec, "cuda")
         q = window_q(case, 80)
         with pytest.raises(RuntimeError, match="fd_prefill"):
