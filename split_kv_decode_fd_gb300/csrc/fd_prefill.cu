@@ -11,7 +11,8 @@
 // One CTA per (batch, pair of query heads of one GQA group -- or one head when
 // the group size is odd --, tile of kPrefillRows = 128 query rows), ten warps:
 //   warp 0    TMA producer: 64-key K and V tiles (16-row x 128-byte boxes, the
-//             128-byte swizzle) into a 2-stage ring, shared by both heads;
+//             128-byte swizzle) into a 3-stage ring (4 for D = 64), shared by
+//             both heads;
 //   warp 1    allocates all 512 TMEM columns and issues tcgen05.mma from one
 //             thread, per head: S = Q K^T (M=128, N=64, K=128) into one of two
 //             TMEM buffers, then O += P V (M=128, N=128, K=64) into its TMEM
@@ -56,11 +57,15 @@ struct PLayout {
   static constexpr uint32_t kTileBytes = kNB * 8192u;           // [kNB][64 rows][128 B]
   static constexpr uint32_t kStageBytes = 2 * kTileBytes;       // K then V
   static constexpr uint32_t kStage0 = 2 * kQGroupBytes;
-  static constexpr uint32_t kBarOff = kStage0 + 2 * kStageBytes;
+  // K/V stages in flight: tile j loads once tile j - kStages is consumed, so the
+  // load latency hides behind the tiles in between (2 stages left it exposed)
+  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr uint32_t kBarOff = kStage0 + kStages * kStageBytes;
   // at least 116 KB, so that one CTA fits per SM: each allocates all 512 TMEM columns
   static constexpr uint32_t kSmemNeed = kBarOff + 256 + 1024;
   static constexpr uint32_t kSmemAlloc = kSmemNeed > 118784u ? kSmemNeed : 118784u;
   static_assert(D == 64 || D == 128, "head dim");
+  static_assert(kSmemAlloc <= 232448, "shared memory");
 };
 
 // ---------------------------------------------------------------- tcgen05
@@ -227,22 +232,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int kStages = Lay::kStages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* kv_full = bars;        // [2 stages]
-  uint64_t* kv_empty = bars + 2;   // [2 stages]
+  uint64_t* kv_full = bars;        // [kStages <= 4]
+  uint64_t* kv_empty = bars + 4;   // [kStages <= 4]
   // Every barrier a waiter might fall behind on alternates between two
   // instances (tile g uses instance g % 2, phase g / 2), so that no barrier can
   // complete two phases ahead of a parity wait: S of tile g+1 is issued before
   // the MMA thread waits for P of tile g, so a fast softmax group may finish
   // tiles g and g+1 meanwhile.
-  uint64_t* s_full = bars + 4;     // [2 groups][2]
-  uint64_t* p_full = bars + 8;     // [2 groups][2]
-  uint64_t* o_done = bars + 12;    // [2 groups][2]
-  uint64_t* o_final = bars + 16;   // [2 groups]: an item's last P.V has completed
-  uint64_t* q_ready = bars + 18;   // an item's q tiles are in shared memory
-  uint64_t* drain = bars + 19;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 160);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 164);
+  uint64_t* s_full = bars + 8;     // [2 groups][2]
+  uint64_t* p_full = bars + 12;    // [2 groups][2]
+  uint64_t* o_done = bars + 16;    // [2 groups][2]
+  uint64_t* o_final = bars + 20;   // [2 groups]: an item's last P.V has completed
+  uint64_t* q_ready = bars + 22;   // an item's q tiles are in shared memory
+  uint64_t* drain = bars + 23;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 196);
 
   // Two query heads of one GQA group share an item (and every K/V tile) when
   // the group size is even; otherwise the second softmax group idles.
@@ -251,11 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t n_items = n_m * (p.Hq / ngroups) * p.B;
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(kv_full + i, 1);
       mbar_init(kv_empty + i, 1);
-      mbar_init(o_final + i, 1);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(o_final + i, 1);
     for (int i = 0; i < 4; ++i) {
       mbar_init(s_full + i, 1);
       mbar_init(p_full + i, 4);
@@ -288,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int32_t idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
       const Item it = item_of(p, idx, ngroups, n_m);
       for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
-        const uint32_t stage = g & 1, use = g >> 1;
+        const uint32_t stage = g % kStages, use = g / kStages;
         if (lane == 0 && (*abort_flag || !mbar_wait(kv_empty + stage, (use & 1) ^ 1))) ok = false;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -324,9 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) *abort_flag = 1;
     // do not leave while this warp's copies may still be landing
     if (lane == 0) {
-      const uint32_t first = g > 2 ? g - 2 : 0;
+      const uint32_t first = g > (uint32_t)kStages ? g - kStages : 0;
       for (uint32_t t = first; t < g; ++t)
-        if (!mbar_wait(kv_full + (t & 1), (t >> 1) & 1)) atomicOr(p.err, kErrTimeout);
+        if (!mbar_wait(kv_full + t % kStages, (t / kStages) & 1)) atomicOr(p.err, kErrTimeout);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -345,8 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int32_t j = 0; j <= n && ok; ++j) {
           if (j < n) {
-            const uint32_t gj = g + j, stage = gj & 1;
-            if (*abort_flag || !mbar_wait(kv_full + stage, (gj >> 1) & 1)) {
+            const uint32_t gj = g + j, stage = gj % kStages;
+            if (*abort_flag || !mbar_wait(kv_full + stage, (gj / kStages) & 1)) {
               ok = false;
               break;
             }
@@ -370,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (j >= 1) {
-            const uint32_t gj = g + j - 1, stage = gj & 1;
+            const uint32_t gj = g + j - 1, stage = gj % kStages;
             const uint32_t vt = sbase + kStage0 + stage * kStageBytes + kTileBytes;
             for (int G = 0; G < ngroups && ok; ++G) {
               if (*abort_flag || !mbar_wait(p_full + G * 2 + (gj & 1), (gj >> 1) & 1)) {
@@ -513,8 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (G == 0 && j == n - 1 && it.L - j * kN < kN) {
           // keys past L in the last tile get p = 0, but 0 * NaN is NaN: zero those V
           // rows (group 0 does it for both: its P.V is issued first)
-          const uint32_t stage = gj & 1;
-          if (ok && (*abort_flag || !mbar_wait(kv_full + stage, (gj >> 1) & 1))) ok = false;
+          const uint32_t stage = gj % kStages;
+          if (ok && (*abort_flag || !mbar_wait(kv_full + stage, (gj / kStages) & 1))) ok = false;
           const int32_t nvalid = it.L - j * kN;
           const uint32_t vt = sbase + kStage0 + stage * kStageBytes + kTileBytes;
           const int32_t tid2 = (warp - 2) * 32 + lane;
