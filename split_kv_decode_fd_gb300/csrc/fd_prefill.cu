@@ -69,17 +69,18 @@ struct PLayout {
 };
 
 // ---------------------------------------------------------------- tcgen05
-// Shared-memory matrix descriptor (sm_100 family): start address, leading and
-// stride byte offsets (all >> 4), version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
+// Shared-memory matrix descriptor (sm_100 family): bits 0-13 start address >> 4,
+// 16-29 leading byte offset >> 4, 32-45 stride byte offset >> 4, 46 version 1,
+// 61-63 swizzle mode (2 = 128-byte swizzle).
+// Built in halves: the high word (stride byte offset 1024,
+// version, swizzle) is a constant here; the low word holds the start address
+// and the leading byte offset, so stepping through a tile is a 32-bit add on
+// the low word (addresses stay below 256 KB: the 14-bit field never carries).
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
+__device__ __forceinline__ uint64_t desc_of(uint32_t lo) { return ((uint64_t)kDescHi << 32) | lo; }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major.
 __host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool b_mn_major) {
@@ -357,19 +358,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t kt = sbase + kStage0 + stage * kStageBytes;
+            const uint32_t k_lo = desc_lo(sbase + kStage0 + stage * kStageBytes, 0);
             for (int G = 0; G < ngroups; ++G) {
               const uint32_t d = tmem + (uint32_t)G * 256u + (gj & 1) * kN;
+              const uint32_t q_lo = desc_lo(sbase + (uint32_t)G * kQGroupBytes, 0);
 #pragma unroll
               for (int part = 0; part < 2; ++part) {
-                const uint32_t qt = sbase + (uint32_t)G * kQGroupBytes + (part ? kQlo : kQhi);
 #pragma unroll
                 for (int s8 = 0; s8 < kD / 16; ++s8) {
-                  const uint32_t off = (uint32_t)(s8 >> 2) * 8192u + (uint32_t)(s8 & 3) * 32u;
-                  const uint64_t a =
-                      smem_desc(qt + (uint32_t)(s8 >> 2) * 16384u + (uint32_t)(s8 & 3) * 32u, 0, 1024);
-                  const uint64_t bd = smem_desc(kt + off, 0, 1024);
-                  umma(d, a, bd, idS, (part | s8) != 0);
+                  // k-step s8: column block s8 / 4, 32 bytes into it per step
+                  const uint32_t a_off = ((part ? kQlo : kQhi) + (uint32_t)(s8 >> 2) * 16384u + (uint32_t)(s8 & 3) * 32u) >> 4;
+                  const uint32_t b_off = ((uint32_t)(s8 >> 2) * 8192u + (uint32_t)(s8 & 3) * 32u) >> 4;
+                  umma(d, desc_of(q_lo + a_off), desc_of(k_lo + b_off), idS, (part | s8) != 0);
                 }
               }
               umma_commit(s_full + G * 2 + (gj & 1));
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (j >= 1) {
             const uint32_t gj = g + j - 1, stage = gj % kStages;
-            const uint32_t vt = sbase + kStage0 + stage * kStageBytes + kTileBytes;
+            const uint32_t v_lo = desc_lo(sbase + kStage0 + stage * kStageBytes + kTileBytes, 8192);
             for (int G = 0; G < ngroups && ok; ++G) {
               if (*abort_flag || !mbar_wait(p_full + G * 2 + (gj & 1), (gj >> 1) & 1)) {
                 ok = false;
@@ -389,9 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int part = 0; part < 2; ++part) {
 #pragma unroll
                 for (int kk = 0; kk < kN / 16; ++kk) {
-                  const uint64_t bd = smem_desc(vt + (uint32_t)kk * 2048u, 8192, 1024);
+                  // 16 keys per step: two 8-row groups of V
                   umma_tmem_a(tmem + (uint32_t)G * 256u + 128u, pt + (uint32_t)part * (kN / 2) + (uint32_t)kk * 8u,
-                              bd, idO, ((j - 1) | part | kk) != 0);
+                              desc_of(v_lo + (uint32_t)kk * (2048u >> 4)), idO, ((j - 1) | part | kk) != 0);
                 }
               }
               umma_commit(o_done + G * 2 + (gj & 1));
