@@ -10,22 +10,24 @@
 //
 // One CTA per (batch, pair of query heads of one GQA group -- or one head when
 // the group size is odd --, tile of kPrefillRows = 128 query rows), ten warps:
-//   warp 0    TMA producer: 64-key K and V tiles (16-row x 128-byte boxes, the
-//             128-byte swizzle) into a 3-stage ring (4 for D = 64), shared by
-//             both heads;
+//   warp 0    TMA producer: 128-key K tiles and V tiles (16-row x 128-byte
+//             boxes, the 128-byte swizzle), each into its own slot of a ring of
+//             3 slots (6 for D = 64), shared by both heads;
 //   warp 1    allocates all 512 TMEM columns and issues tcgen05.mma from one
-//             thread, per head: S = Q K^T (M=128, N=64, K=128) into one of two
-//             TMEM buffers, then O += P V (M=128, N=128, K=64) into its TMEM
-//             accumulator;
-//   warps 2-5 and 6-9: the two heads' softmax groups, which take turns with
-//             the tensor core (two warps per SM sub-partition hide each
-//             other's latency).  Thread = query row = TMEM lane; reads S with tcgen05.ld,
-//             masks, keeps the running max and sum, writes P (bf16 hi and lo)
-//             back over its own S columns with tcgen05.st, rescales O in TMEM
-//             when the max moves, and finally writes O / l.
-// P . V takes A = P straight from TMEM, so the softmax of tile j never waits
-// for P . V of tile j - 1 (that one reads the other S buffer) except to
-// rescale O.
+//             thread, per head: S = Q K^T (M=128, N=128, K=D) into the head's
+//             TMEM buffer, O += P V (M=128, N=D, K=128) into its accumulator,
+//             in the order S0(j), PV1(j-1), S1(j), PV0(j), so that while one
+//             head's softmax runs the tensor core works for the other head;
+//   warps 2-5 and 6-9: the two heads' softmax groups.  Thread = query row =
+//             TMEM lane; reads the tile's 128 scores with tcgen05.ld, masks,
+//             keeps the running max and sum, writes P (bf16 hi and lo) back
+//             over the same columns with tcgen05.st, rescales O in TMEM when
+//             the max moves, and finally writes O / l.
+// P . V takes A = P straight from TMEM.  Each head has one S buffer: S of tile
+// j+1 is issued after P . V of tile j, which reads P from that buffer, and the
+// tensor core runs one CTA's MMAs in issue order.  For the same reason the
+// softmax may rescale O as soon as it sees S of tile j: P . V of tile j-1 was
+// issued before that S, and the commit that signals S tracks it too.
 // K and V are bf16, so the products are exact once q and p are bf16: q (times
 // scale*log2 e) and p are split into bf16 hi + lo parts and each product is
 // issued twice (hi, then lo) into the same fp32 accumulator -- two MMAs buy
@@ -44,27 +46,29 @@ constexpr int kN = kPrefillKeys;   // keys per tile
 constexpr int kThreads = 320;      // producer, MMA, two softmax groups of four warps
 constexpr float kTau = 8.0f;
 constexpr float kLn2f = 0.6931471805599453f;
-constexpr uint32_t kTmemCols = 512;  // per group (256 each): S / P at +0 and +64, O (D columns) at +128
+constexpr uint32_t kTmemCols = 512;  // per head (256 each): S / P at +0, O (D columns) at +128
 
 // Shared-memory layout for head dim D (64 or 128), byte offsets from a
 // 1024-aligned base.  A row of D bf16 is D/64 column blocks of 128 bytes.
 template <int D>
 struct PLayout {
   static constexpr int kNB = D / 64;
-  static constexpr uint32_t kQhi = 0;                           // per group: [kNB][128 rows][128 B] hi, then lo
+  static constexpr uint32_t kQhi = 0;                           // per head: [kNB][128 rows][128 B] hi, then lo
   static constexpr uint32_t kQlo = kNB * 16384u;
   static constexpr uint32_t kQGroupBytes = 2 * kQlo;
-  static constexpr uint32_t kTileBytes = kNB * 8192u;           // [kNB][64 rows][128 B]
-  static constexpr uint32_t kStageBytes = 2 * kTileBytes;       // K then V
-  static constexpr uint32_t kStage0 = 2 * kQGroupBytes;
-  // K/V stages in flight: tile j loads once tile j - kStages is consumed, so the
-  // load latency hides behind the tiles in between (2 stages left it exposed)
-  static constexpr int kStages = D == 128 ? 3 : 4;
-  static constexpr uint32_t kBarOff = kStage0 + kStages * kStageBytes;
+  static constexpr uint32_t kTileBytes = kNB * 16384u;          // one K or V tile: [kNB][128 rows][128 B]
+  static constexpr uint32_t kBlockBytes = 16384u;               // one 128-byte column block of a tile
+  static constexpr uint32_t kSlot0 = 2 * kQGroupBytes;
+  // K and V tiles take one slot each, K(j) then V(j); a slot is refilled once
+  // the MMAs reading it have completed.  For D = 128 three slots are what fits
+  // beside the two heads' q (227 KB in all).
+  static constexpr int kSlots = D == 128 ? 3 : 6;
+  static constexpr uint32_t kBarOff = kSlot0 + kSlots * kTileBytes;
   // at least 116 KB, so that one CTA fits per SM: each allocates all 512 TMEM columns
   static constexpr uint32_t kSmemNeed = kBarOff + 256 + 1024;
   static constexpr uint32_t kSmemAlloc = kSmemNeed > 118784u ? kSmemNeed : 118784u;
   static_assert(D == 64 || D == 128, "head dim");
+  static_assert(kSlots <= 8, "barrier area holds 8 slots");
   static_assert(kSmemAlloc <= 232448, "shared memory");
 };
 
@@ -130,6 +134,32 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// The same load without the wait: several may be in flight before one
+// tcgen05.wait::ld.
+__device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive 32-bit columns of this thread's lane (no wait).
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -147,17 +177,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
-      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
-      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
 }
 
 // 2^x on the special-function unit (inputs here are <= 0 or -inf).
@@ -197,7 +216,7 @@ struct Item {
 };
 
 // Items in order of decreasing work (causal: the latest query rows first), so
-// that the persistent CTAs, taking items round-robin, end close together.
+// that the hardware, handing out CTAs in index order, starts the long ones first.
 __device__ __forceinline__ Item item_of(const PrefillParams& p, int32_t idx, int32_t ngroups, int32_t n_m) {
   const int32_t hp = p.Hq / ngroups;
   const int32_t per_m = hp * p.B;
@@ -218,7 +237,8 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int32_t idx, int
 // Each CTA walks items blockIdx.x, + gridDim.x, ... (one item when launched
 // with a CTA per item).  Every role walks the same items, and all barrier
 // phases follow two running counters of the CTA: g, the key tiles processed so
-// far, and f, the items with at least one tile so far.
+// far, and f, the items with at least one tile so far.  Slot uses are numbered
+// u = 2 g (K) and 2 g + 1 (V): slot u % kSlots, phase u / kSlots.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fd_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -227,25 +247,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kD = D;
   constexpr int kNB = Lay::kNB;
   constexpr uint32_t kQhi = Lay::kQhi, kQlo = Lay::kQlo, kQGroupBytes = Lay::kQGroupBytes;
-  constexpr uint32_t kTileBytes = Lay::kTileBytes, kStageBytes = Lay::kStageBytes, kStage0 = Lay::kStage0;
+  constexpr uint32_t kTileBytes = Lay::kTileBytes, kBlockBytes = Lay::kBlockBytes, kSlot0 = Lay::kSlot0;
   constexpr uint32_t kBarOff = Lay::kBarOff;
+  constexpr uint32_t kSlots = (uint32_t)Lay::kSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr int kStages = Lay::kStages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* kv_full = bars;        // [kStages <= 4]
-  uint64_t* kv_empty = bars + 4;   // [kStages <= 4]
-  // Every barrier a waiter might fall behind on alternates between two
-  // instances (tile g uses instance g % 2, phase g / 2), so that no barrier can
-  // complete two phases ahead of a parity wait: S of tile g+1 is issued before
-  // the MMA thread waits for P of tile g, so a fast softmax group may finish
-  // tiles g and g+1 meanwhile.
-  uint64_t* s_full = bars + 8;     // [2 groups][2]
-  uint64_t* p_full = bars + 12;    // [2 groups][2]
-  uint64_t* o_done = bars + 16;    // [2 groups][2]
-  uint64_t* o_final = bars + 20;   // [2 groups]: an item's last P.V has completed
+  uint64_t* kv_full = bars;        // [kSlots <= 8]
+  uint64_t* kv_empty = bars + 8;   // [kSlots <= 8]
+  // One phase per key tile.  Neither side can get two phases ahead: S of tile
+  // j+1 is issued only after P of tile j has arrived, and P of tile j+1 needs
+  // S of tile j+1.
+  uint64_t* s_full = bars + 16;    // [2 heads]
+  uint64_t* p_full = bars + 18;    // [2 heads]
+  uint64_t* o_final = bars + 20;   // [2 heads]: an item's last P.V has completed
   uint64_t* q_ready = bars + 22;   // an item's q tiles are in shared memory
   uint64_t* drain = bars + 23;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 192);
@@ -258,15 +275,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t n_items = n_m * (p.Hq / ngroups) * p.B;
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (uint32_t i = 0; i < kSlots; ++i) {
       mbar_init(kv_full + i, 1);
       mbar_init(kv_empty + i, 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(o_final + i, 1);
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
       mbar_init(p_full + i, 4);
-      mbar_init(o_done + i, 1);
+      mbar_init(o_final + i, 1);
     }
     mbar_init(q_ready, 4 * ngroups);
     mbar_init(drain, 1);
@@ -291,14 +307,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    uint32_t g = 0;
+    uint32_t u = 0;  // slot uses so far
     for (int32_t idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
       const Item it = item_of(p, idx, ngroups, n_m);
       for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
-        const uint32_t stage = g % kStages, use = g / kStages;
-        if (lane == 0 && (*abort_flag || !mbar_wait(kv_empty + stage, (use & 1) ^ 1))) ok = false;
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
+        // lane l brings rows [16 l, 16 l + 16) of the tile: one page run when paged
         const int32_t t0 = j * kN;
         const int32_t nvalid = it.L - t0 < kN ? it.L - t0 : kN;
         const int32_t tok = t0 + 16 * lane;
@@ -314,26 +327,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           z = page * p.Hkv + it.kvh;
         }
         const unsigned issue = __ballot_sync(0xffffffffu, mine);
-        if (lane == 0) mbar_arrive_expect_tx(kv_full + stage, (uint32_t)__popc(issue) * 2u * kNB * 2048u);
-        __syncwarp();
-        if (mine) {
-          uint8_t* kdst = smem + kStage0 + stage * kStageBytes + lane * 2048;
-          uint8_t* vdst = kdst + kTileBytes;
+        for (int kv = 0; kv < 2; ++kv, ++u) {
+          const uint32_t slot = u % kSlots, use = u / kSlots;
+          if (lane == 0 && (*abort_flag || !mbar_wait(kv_empty + slot, (use & 1) ^ 1))) ok = false;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (lane == 0) mbar_arrive_expect_tx(kv_full + slot, (uint32_t)__popc(issue) * kNB * 2048u);
+          __syncwarp();
+          if (mine) {
+            uint8_t* dst = smem + kSlot0 + slot * kTileBytes + lane * 2048;
+            const CUtensorMap* map = kv == 0 ? &tmap_k : &tmap_v;
 #pragma unroll
-          for (int blk = 0; blk < kNB; ++blk) {
-            tma_load_3d(kdst + blk * 8192, &tmap_k, kv_full + stage, blk * 64, row, z);
-            tma_load_3d(vdst + blk * 8192, &tmap_v, kv_full + stage, blk * 64, row, z);
+            for (int blk = 0; blk < kNB; ++blk) tma_load_3d(dst + blk * kBlockBytes, map, kv_full + slot, blk * 64, row, z);
           }
         }
-        ++g;
       }
     }
     if (!ok) *abort_flag = 1;
     // do not leave while this warp's copies may still be landing
     if (lane == 0) {
-      const uint32_t first = g > (uint32_t)kStages ? g - kStages : 0;
-      for (uint32_t t = first; t < g; ++t)
-        if (!mbar_wait(kv_full + t % kStages, (t / kStages) & 1)) atomicOr(p.err, kErrTimeout);
+      const uint32_t first = u > kSlots ? u - kSlots : 0;
+      for (uint32_t t = first; t < u; ++t)
+        if (!mbar_wait(kv_full + t % kSlots, (t / kSlots) & 1)) atomicOr(p.err, kErrTimeout);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -341,67 +356,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idS = instr_desc(kM, kN, false);
       constexpr uint32_t idO = instr_desc(kM, kD, true);
       uint32_t g = 0, f = 0;
+      // S_G = Q_G K^T for the K tile in slot `slot`: D/16 k-steps, hi then lo
+      auto issue_s = [&](int G, uint32_t slot) {
+        const uint32_t d = tmem + (uint32_t)G * 256u;
+        const uint32_t q_lo = desc_lo(sbase + (uint32_t)G * kQGroupBytes, 0);
+        const uint32_t k_lo = desc_lo(sbase + kSlot0 + slot * kTileBytes, 0);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+          for (int s8 = 0; s8 < kD / 16; ++s8) {
+            // k-step s8: column block s8 / 4, 32 bytes into it per step
+            const uint32_t a_off = ((part ? kQlo : kQhi) + (uint32_t)(s8 >> 2) * 16384u + (uint32_t)(s8 & 3) * 32u) >> 4;
+            const uint32_t b_off = ((uint32_t)(s8 >> 2) * kBlockBytes + (uint32_t)(s8 & 3) * 32u) >> 4;
+            umma(d, desc_of(q_lo + a_off), desc_of(k_lo + b_off), idS, (part | s8) != 0);
+          }
+        }
+        umma_commit(s_full + G);
+      };
+      // O_G += P_G V for the V tile in slot `slot`: 16 keys per k-step (two
+      // 8-row groups of V), P hi in S columns [0, 64), lo in [64, 128)
+      auto issue_pv = [&](int G, uint32_t slot, bool first) {
+        const uint32_t pt = tmem + (uint32_t)G * 256u;
+        const uint32_t v_lo = desc_lo(sbase + kSlot0 + slot * kTileBytes, kBlockBytes);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+          for (int kk = 0; kk < kN / 16; ++kk) {
+            umma_tmem_a(pt + 128u, pt + (uint32_t)part * (kN / 2) + (uint32_t)kk * 8u,
+                        desc_of(v_lo + (uint32_t)kk * (2048u >> 4)), idO, (!first || part || kk) ? 1u : 0u);
+          }
+        }
+      };
+      auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
+        if (*abort_flag || !mbar_wait(bar, parity)) ok = false;
+        tc_fence_after();
+        return ok;
+      };
       for (int32_t idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
         const Item it = item_of(p, idx, ngroups, n_m);
         const int32_t n = it.n_tiles;
         if (n == 0) continue;  // no q_ready phase either: the softmax skips such items too
-        if (*abort_flag || !mbar_wait(q_ready, f & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int32_t j = 0; j <= n && ok; ++j) {
-          if (j < n) {
-            const uint32_t gj = g + j, stage = gj % kStages;
-            if (*abort_flag || !mbar_wait(kv_full + stage, (gj / kStages) & 1)) {
-              ok = false;
-              break;
+        if (!wait_bar(q_ready, f & 1)) break;
+        for (int32_t j = 0; j < n; ++j) {
+          const uint32_t gj = g + (uint32_t)j;
+          const uint32_t uk = 2 * gj, uv = uk + 1;
+          if (!wait_bar(kv_full + uk % kSlots, (uk / kSlots) & 1)) break;
+          issue_s(0, uk % kSlots);
+          if (ngroups == 2) {
+            if (j >= 1) {
+              // head 1's P.V of the previous tile, then its S of this tile
+              if (!wait_bar(p_full + 1, (gj - 1) & 1)) break;
+              issue_pv(1, (uv - 2) % kSlots, j == 1);
+              umma_commit(kv_empty + (uv - 2) % kSlots);
             }
-            tc_fence_after();
-            const uint32_t k_lo = desc_lo(sbase + kStage0 + stage * kStageBytes, 0);
-            for (int G = 0; G < ngroups; ++G) {
-              const uint32_t d = tmem + (uint32_t)G * 256u + (gj & 1) * kN;
-              const uint32_t q_lo = desc_lo(sbase + (uint32_t)G * kQGroupBytes, 0);
-#pragma unroll
-              for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                for (int s8 = 0; s8 < kD / 16; ++s8) {
-                  // k-step s8: column block s8 / 4, 32 bytes into it per step
-                  const uint32_t a_off = ((part ? kQlo : kQhi) + (uint32_t)(s8 >> 2) * 16384u + (uint32_t)(s8 & 3) * 32u) >> 4;
-                  const uint32_t b_off = ((uint32_t)(s8 >> 2) * 8192u + (uint32_t)(s8 & 3) * 32u) >> 4;
-                  umma(d, desc_of(q_lo + a_off), desc_of(k_lo + b_off), idS, (part | s8) != 0);
-                }
-              }
-              umma_commit(s_full + G * 2 + (gj & 1));
-            }
+            issue_s(1, uk % kSlots);
           }
-          if (j >= 1) {
-            const uint32_t gj = g + j - 1, stage = gj % kStages;
-            const uint32_t v_lo = desc_lo(sbase + kStage0 + stage * kStageBytes + kTileBytes, 8192);
-            for (int G = 0; G < ngroups && ok; ++G) {
-              if (*abort_flag || !mbar_wait(p_full + G * 2 + (gj & 1), (gj >> 1) & 1)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint32_t pt = tmem + (uint32_t)G * 256u + (gj & 1) * kN;  // P hi [0, 32), lo [32, 64)
-#pragma unroll
-              for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                for (int kk = 0; kk < kN / 16; ++kk) {
-                  // 16 keys per step: two 8-row groups of V
-                  umma_tmem_a(tmem + (uint32_t)G * 256u + 128u, pt + (uint32_t)part * (kN / 2) + (uint32_t)kk * 8u,
-                              desc_of(v_lo + (uint32_t)kk * (2048u >> 4)), idO, ((j - 1) | part | kk) != 0);
-                }
-              }
-              umma_commit(o_done + G * 2 + (gj & 1));
-              if (j == n) umma_commit(o_final + G);
-            }
-            if (!ok) break;
-            umma_commit(kv_empty + stage);
-          }
+          umma_commit(kv_empty + uk % kSlots);
+          if (!wait_bar(kv_full + uv % kSlots, (uv / kSlots) & 1)) break;
+          if (!wait_bar(p_full + 0, gj & 1)) break;
+          issue_pv(0, uv % kSlots, j == 0);
+          if (j == n - 1) umma_commit(o_final + 0);
+          if (ngroups == 1) umma_commit(kv_empty + uv % kSlots);
         }
-        g += n;
+        if (!ok) break;
+        if (ngroups == 2) {
+          const uint32_t gl = g + (uint32_t)n - 1, uv = 2 * gl + 1;
+          if (!wait_bar(p_full + 1, gl & 1)) break;
+          issue_pv(1, uv % kSlots, n == 1);
+          umma_commit(kv_empty + uv % kSlots);
+          umma_commit(o_final + 1);
+        }
+        g += (uint32_t)n;
         ++f;
       }
       if (!ok) {
@@ -413,13 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(drain, 0)) atomicOr(p.err, kErrTimeout);
     }
   } else if ((warp - 2) / 4 < ngroups) {
-    // ------------------------------------------------------------ softmax, group G
+    // ------------------------------------------------------------ softmax, head G
     const int32_t G = (warp - 2) / 4;
     const int32_t quarter = warp & 3;
     const int32_t r = quarter * 32 + lane;  // query row in the tile = TMEM lane
     const uint32_t tbase = tmem + (uint32_t)G * 256u + ((uint32_t)(quarter * 32) << 16);
     const uint32_t qbase = sbase + (uint32_t)G * kQGroupBytes;
-    uint64_t* my_s_full = s_full + G * 2;
     uint32_t g = 0, f = 0;
     for (int32_t idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
       const Item it = item_of(p, idx, ngroups, n_m);
@@ -429,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t lim = row_keys(p, it.L, qi);
       if (n > 0) {
         // q row, times scale*log2(e), as bf16 hi / lo in the swizzled A layout.  The
-        // previous item's MMAs are all complete (its epilogue waited o_final).
+        // previous item's S MMAs are all complete (this group saw its last S).
         const float* qrow = p.q + (((size_t)it.b * p.Hq + h) * p.n_q + (qi < p.n_q ? qi : 0)) * kD;
 #pragma unroll 8
         for (int c = 0; c < kD / 8; ++c) {
@@ -459,19 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // all 128 threads of the group): later waits are skipped, the output flagged.
       float mref = -INFINITY, l = 0.f;
       for (int32_t j = 0; j < n; ++j) {
-        const uint32_t gj = g + j;
-        if (ok && (*abort_flag || !mbar_wait(my_s_full + (gj & 1), (gj >> 1) & 1))) ok = false;
+        const uint32_t gj = g + (uint32_t)j;
+        if (ok && (*abort_flag || !mbar_wait(s_full + G, gj & 1))) ok = false;
         tc_fence_after();
         float s[kN];
-        {
-          float a[32];
-          tmem_ld32(tbase + (gj & 1) * kN, a);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) s[c] = a[c];
-          tmem_ld32(tbase + (gj & 1) * kN + 32, a);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) s[32 + c] = a[c];
-        }
+        for (int c = 0; c < kN / 32; ++c) tmem_ld32_nw(tbase + (uint32_t)c * 32u, s + 32 * c);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         // mask the keys past this row's limit (only the tiles that reach it)
         const int32_t keys_left = lim - j * kN;
         if (keys_left < kN) {
@@ -489,24 +507,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha = mref == -INFINITY ? 0.f : ex2(mref - mn);
           mref = mn;
         }
+        // p = 2^(s - max), and P over this tile's S columns, 32 keys at a time:
+        // hi in [0, 64), lo in [64, 128), two keys per column.  The whole tile's
+        // S is in registers already, so the stores may overwrite any of it.
         const float base = mref == -INFINITY ? 0.f : mref;
         float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < kN; ++c) {
-          s[c] = ex2(s[c] - base);
-          sum4[c & 3] += s[c];
+        for (int c = 0; c < kN / 32; ++c) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2(s[32 * c + 2 * e] - base), p1 = ex2(s[32 * c + 2 * e + 1] - base);
+            sum4[(2 * e) & 3] += p0;
+            sum4[(2 * e + 1) & 3] += p1;
+            split2(p0, p1, hi[e], lo[e]);
+          }
+          tmem_st16u(tbase + (uint32_t)c * 16u, hi);
+          tmem_st16u(tbase + (uint32_t)(kN / 2) + (uint32_t)c * 16u, lo);
         }
         l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-        // Rescaling O needs the previous tile's P.V to have finished.  tcgen05.ld
-        // and st are warp-collective (.sync.aligned): the whole warp rescales
-        // when any of its rows must, the others with alpha = 1.  P.V of tile g-1
-        // completes phase (g-1)/2 of o_done[G][(g-1)%2]; a parity wait for it is
-        // exact although earlier phases were not waited: that barrier's previous
-        // phase (tile g-3) finished before this tile's S (issued after it, in
-        // order), and its next one (tile g+1) needs this group's P first.
+        // Rescaling O needs the previous tile's P.V to have finished: it was
+        // issued before this tile's S, whose completion this group just saw.
+        // tcgen05.ld and st are warp-collective (.sync.aligned): the whole warp
+        // rescales when any of its rows must, the others with alpha = 1.
         if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
-          if (ok && (*abort_flag || !mbar_wait(o_done + G * 2 + ((gj - 1) & 1), ((gj - 1) >> 1) & 1))) ok = false;
-          tc_fence_after();
 #pragma unroll 1
           for (int c4 = 0; c4 < kD / 32; ++c4) {
             float o[32];
@@ -518,32 +542,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (G == 0 && j == n - 1 && it.L - j * kN < kN) {
           // keys past L in the last tile get p = 0, but 0 * NaN is NaN: zero those V
-          // rows (group 0 does it for both: its P.V is issued first)
-          const uint32_t stage = gj % kStages;
-          if (ok && (*abort_flag || !mbar_wait(kv_full + stage, (gj / kStages) & 1))) ok = false;
+          // rows (head 0 does it for both: its P.V is issued first)
+          const uint32_t uv = 2 * gj + 1, slot = uv % kSlots;
+          if (ok && (*abort_flag || !mbar_wait(kv_full + slot, (uv / kSlots) & 1))) ok = false;
           const int32_t nvalid = it.L - j * kN;
-          const uint32_t vt = sbase + kStage0 + stage * kStageBytes + kTileBytes;
+          const uint32_t vt = sbase + kSlot0 + slot * kTileBytes;
           const int32_t tid2 = (warp - 2) * 32 + lane;
           constexpr int kRowChunks = kD * 2 / 16;
           for (int32_t e = tid2; e < (kN - nvalid) * kRowChunks; e += 128) {
             const uint32_t row = (uint32_t)(nvalid + e / kRowChunks), c = (uint32_t)(e % kRowChunks);
-            sts128(vt + (c >> 3) * 8192u + row * 128u + ((c & 7u) << 4), 0u, 0u, 0u, 0u);
+            sts128(vt + (c >> 3) * kBlockBytes + row * 128u + ((c & 7u) << 4), 0u, 0u, 0u, 0u);
           }
         }
-        // P over this tile's S columns: hi in [0, 32), lo in [32, 64), two keys per column
-        {
-          uint32_t hi[32], lo[32];
-#pragma unroll
-          for (int c = 0; c < kN / 2; ++c) split2(s[2 * c], s[2 * c + 1], hi[c], lo[c]);
-          const uint32_t pt = tbase + (gj & 1) * kN;
-          tmem_st32u(pt, hi);
-          tmem_st32u(pt + kN / 2, lo);
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the zeroed V rows, if any
         tc_fence_before();
         named_barrier(1 + G, 128);  // every thread of the group has stored before the arrival
-        if (lane == 0) mbar_arrive(p_full + G * 2 + (gj & 1));
+        if (lane == 0) mbar_arrive(p_full + G);
       }
       // ---- epilogue: out = O / l, lse = ln(sum of exp).  n is the same for the
       // whole CTA, so the collective loads run on every lane or none.
@@ -574,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this group's O columns are read before the next item's first P.V (which
       // needs this group's P) overwrites them
       tc_fence_before();
-      g += n;
+      g += (uint32_t)n;
       if (n > 0) ++f;
     }
     if (!ok) {

@@ -22,7 +22,7 @@ struct PrefillParams {
 
 // Query rows per CTA and keys per tile of the prefill kernel.
 constexpr int kPrefillRows = 128;
-constexpr int kPrefillKeys = 64;
+constexpr int kPrefillKeys = 128;
 
 // D = 64 or 128; cudaErrorInvalidValue otherwise.
 cudaError_t launch_prefill(int D, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
