@@ -54,6 +54,8 @@ def parse_args():
                     help="time K plain stream launches instead of one CUDA graph of K launches")
     ap.add_argument("--prefill", type=int, default=0, metavar="N",
                     help="time fd_prefill on an N-token causal prompt (B=1, Hq=32, Hkv=8, D=128): TFLOP/s")
+    ap.add_argument("--prefill-kv-heads", type=int, default=8, metavar="HKV",
+                    help="KV heads of the --prefill prompt (32 = MHA; 32 must be a multiple)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -565,8 +567,10 @@ def run_prefill(args):
     import split_kv_decode_fd_gb300 as fd
     from workloads import make_case, small_spec
     fd.load_library()
-    N = args.prefill
-    spec = small_spec(f"prefill_causal_B1_Hq32_Hkv8_N{N}", 1, 32, 8, 128, N, seed=1003)
+    N, hkv = args.prefill, args.prefill_kv_heads
+    if hkv < 1 or 32 % hkv:
+        raise SystemExit("--prefill-kv-heads must divide 32")
+    spec = small_spec(f"prefill_causal_B1_Hq32_Hkv{hkv}_N{N}", 1, 32, hkv, 128, N, seed=1003)
     case = make_case(spec, device)
     gen = torch.Generator(device=device).manual_seed(spec.seed + 31)
     q = torch.randn((1, 32, N, 128), generator=gen, device=device)
@@ -638,7 +642,7 @@ def run_prefill(args):
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16x2 (hi+lo) -> f32",
         "data": "synthetic",
-        "config": {"workload": spec.name, "B": 1, "Hq": 32, "Hkv": 8, "D": 128, "n_q": N, "keys": N,
+        "config": {"workload": spec.name, "B": 1, "Hq": 32, "Hkv": hkv, "D": 128, "n_q": N, "keys": N,
                    "causal": True, "kv_dtype": "bf16", "q_dtype": "f32", "flops_per_step": flops,
                    "launch": "one CUDA graph of K fd_prefill calls",
                    "kernel": "fd_prefill_kernel (tcgen05.mma M=128; q and p as bf16 hi+lo: 2 MMAs per product)"},

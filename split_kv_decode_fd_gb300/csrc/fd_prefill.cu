@@ -210,6 +210,13 @@ __device__ __forceinline__ int32_t row_keys(const PrefillParams& p, int32_t L, i
   return lim < 0 ? 0 : (lim > L ? L : lim);
 }
 
+// The MMA thread's waits: false when the CTA aborts or the wait times out.
+__device__ __forceinline__ bool wait_ok(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const bool r = !*abort_flag && mbar_wait(bar, parity);
+  tc_fence_after();
+  return r;
+}
+
 // One work item: a tile of kM query rows of one sequence for `ngroups` heads.
 struct Item {
   int32_t b, h0, m0, kvh, L, n_tiles;
@@ -257,19 +264,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint64_t* kv_full = bars;        // [kSlots <= 8]
   uint64_t* kv_empty = bars + 8;   // [kSlots <= 8]
-  // One phase per key tile.  Neither side can get two phases ahead: S of tile
-  // j+1 is issued only after P of tile j has arrived, and P of tile j+1 needs
-  // S of tile j+1.
-  uint64_t* s_full = bars + 16;    // [2 heads]
-  uint64_t* p_full = bars + 18;    // [2 heads]
+  // One phase per key tile and S buffer.  Neither side can get two phases
+  // ahead: S into a buffer is issued only after the P that the buffer last
+  // held has arrived, and that P needed the S before it.
+  uint64_t* s_full = bars + 16;    // [2 buffers]
+  uint64_t* p_full = bars + 18;    // [2 buffers]
   uint64_t* o_final = bars + 20;   // [2 heads]: an item's last P.V has completed
   uint64_t* q_ready = bars + 22;   // an item's q tiles are in shared memory
   uint64_t* drain = bars + 23;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 192);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 196);
+  uint64_t* o_done = bars + 24;    // one head per CTA only: a P.V has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 208);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 212);
 
   // Two query heads of one GQA group share an item (and every K/V tile) when
-  // the group size is even; otherwise the second softmax group idles.
+  // the group size is even: head G has S buffer G (TMEM columns 256 G) and O
+  // at 256 G + 128.  Otherwise the second softmax group idles and the one head
+  // alternates between both S buffers, tile by tile, so that S of tile j+1 is
+  // computed while the softmax works on tile j.
   const int32_t ngroups = (p.g % 2 == 0) ? 2 : 1;
   const int32_t n_m = (p.n_q + kM - 1) / kM;
   const int32_t n_items = n_m * (p.Hq / ngroups) * p.B;
@@ -286,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(q_ready, 4 * ngroups);
     mbar_init(drain, 1);
+    mbar_init(o_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -356,9 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idS = instr_desc(kM, kN, false);
       constexpr uint32_t idO = instr_desc(kM, kD, true);
       uint32_t g = 0, f = 0;
-      // S_G = Q_G K^T for the K tile in slot `slot`: D/16 k-steps, hi then lo
-      auto issue_s = [&](int G, uint32_t slot) {
-        const uint32_t d = tmem + (uint32_t)G * 256u;
+      // S = Q_G K^T into TMEM column `d_col`, for the K tile in slot `slot`:
+      // D/16 k-steps, hi then lo
+      auto issue_s = [=](uint32_t d_col, int G, uint32_t slot) {
+        const uint32_t d = tmem + d_col;
         const uint32_t q_lo = desc_lo(sbase + (uint32_t)G * kQGroupBytes, 0);
         const uint32_t k_lo = desc_lo(sbase + kSlot0 + slot * kTileBytes, 0);
 #pragma unroll
@@ -371,60 +384,95 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma(d, desc_of(q_lo + a_off), desc_of(k_lo + b_off), idS, (part | s8) != 0);
           }
         }
-        umma_commit(s_full + G);
       };
-      // O_G += P_G V for the V tile in slot `slot`: 16 keys per k-step (two
-      // 8-row groups of V), P hi in S columns [0, 64), lo in [64, 128)
-      auto issue_pv = [&](int G, uint32_t slot, bool first) {
-        const uint32_t pt = tmem + (uint32_t)G * 256u;
+      // O (TMEM column o_col) += P V, P at column p_col, for the V tile in slot
+      // `slot`: 16 keys per k-step (two 8-row groups of V), P hi in the buffer's
+      // columns [0, 64), lo in [64, 128)
+      auto issue_pv = [=](uint32_t p_col, uint32_t o_col, uint32_t slot, bool first) {
         const uint32_t v_lo = desc_lo(sbase + kSlot0 + slot * kTileBytes, kBlockBytes);
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
           for (int kk = 0; kk < kN / 16; ++kk) {
-            umma_tmem_a(pt + 128u, pt + (uint32_t)part * (kN / 2) + (uint32_t)kk * 8u,
+            umma_tmem_a(tmem + o_col, tmem + p_col + (uint32_t)part * (kN / 2) + (uint32_t)kk * 8u,
                         desc_of(v_lo + (uint32_t)kk * (2048u >> 4)), idO, (!first || part || kk) ? 1u : 0u);
           }
         }
-      };
-      auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
-        if (*abort_flag || !mbar_wait(bar, parity)) ok = false;
-        tc_fence_after();
-        return ok;
       };
       for (int32_t idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
         const Item it = item_of(p, idx, ngroups, n_m);
         const int32_t n = it.n_tiles;
         if (n == 0) continue;  // no q_ready phase either: the softmax skips such items too
-        if (!wait_bar(q_ready, f & 1)) break;
-        for (int32_t j = 0; j < n; ++j) {
-          const uint32_t gj = g + (uint32_t)j;
-          const uint32_t uk = 2 * gj, uv = uk + 1;
-          if (!wait_bar(kv_full + uk % kSlots, (uk / kSlots) & 1)) break;
-          issue_s(0, uk % kSlots);
-          if (ngroups == 2) {
+        if (!wait_ok(q_ready, f & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (ngroups == 2) {
+          for (int32_t j = 0; j < n; ++j) {
+            const uint32_t gj = g + (uint32_t)j;
+            const uint32_t uk = 2 * gj, uv = uk + 1;
+            if (!wait_ok(kv_full + uk % kSlots, (uk / kSlots) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            issue_s(0, 0, uk % kSlots);
+            umma_commit(s_full + 0);
             if (j >= 1) {
               // head 1's P.V of the previous tile, then its S of this tile
-              if (!wait_bar(p_full + 1, (gj - 1) & 1)) break;
-              issue_pv(1, (uv - 2) % kSlots, j == 1);
+              if (!wait_ok(p_full + 1, (gj - 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              issue_pv(256, 384, (uv - 2) % kSlots, j == 1);
               umma_commit(kv_empty + (uv - 2) % kSlots);
             }
-            issue_s(1, uk % kSlots);
+            issue_s(256, 1, uk % kSlots);
+            umma_commit(s_full + 1);
+            umma_commit(kv_empty + uk % kSlots);
+            if (!wait_ok(kv_full + uv % kSlots, (uv / kSlots) & 1, abort_flag) ||
+                !wait_ok(p_full + 0, gj & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            issue_pv(0, 128, uv % kSlots, j == 0);
+            if (j == n - 1) umma_commit(o_final + 0);
           }
-          umma_commit(kv_empty + uk % kSlots);
-          if (!wait_bar(kv_full + uv % kSlots, (uv / kSlots) & 1)) break;
-          if (!wait_bar(p_full + 0, gj & 1)) break;
-          issue_pv(0, uv % kSlots, j == 0);
-          if (j == n - 1) umma_commit(o_final + 0);
-          if (ngroups == 1) umma_commit(kv_empty + uv % kSlots);
-        }
-        if (!ok) break;
-        if (ngroups == 2) {
+          if (!ok) break;
           const uint32_t gl = g + (uint32_t)n - 1, uv = 2 * gl + 1;
-          if (!wait_bar(p_full + 1, gl & 1)) break;
-          issue_pv(1, uv % kSlots, n == 1);
+          if (!wait_ok(p_full + 1, gl & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          issue_pv(256, 384, uv % kSlots, n == 1);
           umma_commit(kv_empty + uv % kSlots);
           umma_commit(o_final + 1);
+        } else {
+          // one head: S(j) into buffer j % 2, then P.V of tile j-1
+          for (int32_t j = 0; j <= n; ++j) {
+            if (j < n) {
+              const uint32_t gj = g + (uint32_t)j, uk = 2 * gj;
+              if (!wait_ok(kv_full + uk % kSlots, (uk / kSlots) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              issue_s((gj & 1) * 256u, 0, uk % kSlots);
+              umma_commit(s_full + (gj & 1));
+              umma_commit(kv_empty + uk % kSlots);
+            }
+            if (j >= 1) {
+              const uint32_t gp = g + (uint32_t)j - 1, uv = 2 * gp + 1;
+              if (!wait_ok(kv_full + uv % kSlots, (uv / kSlots) & 1, abort_flag) ||
+                  !wait_ok(p_full + (gp & 1), (gp >> 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              issue_pv((gp & 1) * 256u, 128, uv % kSlots, j == 1);
+              umma_commit(o_done);
+              umma_commit(kv_empty + uv % kSlots);
+              if (j == n) umma_commit(o_final + 0);
+            }
+          }
+          if (!ok) break;
         }
         g += (uint32_t)n;
         ++f;
@@ -442,7 +490,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t G = (warp - 2) / 4;
     const int32_t quarter = warp & 3;
     const int32_t r = quarter * 32 + lane;  // query row in the tile = TMEM lane
-    const uint32_t tbase = tmem + (uint32_t)G * 256u + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t obase = tmem + (uint32_t)G * 256u + 128u + lane_off;  // this head's O
+    const bool dual = ngroups == 1;  // one head, alternating S buffers
     const uint32_t qbase = sbase + (uint32_t)G * kQGroupBytes;
     uint32_t g = 0, f = 0;
     for (int32_t idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
@@ -484,7 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mref = -INFINITY, l = 0.f;
       for (int32_t j = 0; j < n; ++j) {
         const uint32_t gj = g + (uint32_t)j;
-        if (ok && (*abort_flag || !mbar_wait(s_full + G, gj & 1))) ok = false;
+        const uint32_t buf = dual ? (gj & 1) : (uint32_t)G, par = dual ? (gj >> 1) & 1 : gj & 1;
+        const uint32_t tbase = tmem + buf * 256u + lane_off;  // this tile's S / P
+        if (ok && (*abort_flag || !mbar_wait(s_full + buf, par))) ok = false;
         tc_fence_after();
         float s[kN];
 #pragma unroll
@@ -526,18 +578,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16u(tbase + (uint32_t)(kN / 2) + (uint32_t)c * 16u, lo);
         }
         l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-        // Rescaling O needs the previous tile's P.V to have finished: it was
-        // issued before this tile's S, whose completion this group just saw.
-        // tcgen05.ld and st are warp-collective (.sync.aligned): the whole warp
-        // rescales when any of its rows must, the others with alpha = 1.
+        // Rescaling O needs the previous tile's P.V to have finished.  With two
+        // heads it was issued before this tile's S, whose completion this group
+        // just saw; with one head it comes after, and o_done tells (a parity
+        // wait is exact: P.V of tile g-2 was issued before this S, and that of
+        // tile g needs this P).  tcgen05.ld and st are warp-collective
+        // (.sync.aligned): the whole warp rescales when any of its rows must,
+        // the others with alpha = 1.
         if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+          if (dual && ok && (*abort_flag || !mbar_wait(o_done, (gj - 1) & 1))) ok = false;
+          tc_fence_after();
 #pragma unroll 1
           for (int c4 = 0; c4 < kD / 32; ++c4) {
             float o[32];
-            tmem_ld32(tbase + 128 + (uint32_t)c4 * 32, o);
+            tmem_ld32(obase + (uint32_t)c4 * 32, o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(tbase + 128 + (uint32_t)c4 * 32, o);
+            tmem_st32(obase + (uint32_t)c4 * 32, o);
           }
         }
         if (G == 0 && j == n - 1 && it.L - j * kN < kN) {
@@ -558,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the zeroed V rows, if any
         tc_fence_before();
         named_barrier(1 + G, 128);  // every thread of the group has stored before the arrival
-        if (lane == 0) mbar_arrive(p_full + G);
+        if (lane == 0) mbar_arrive(p_full + buf);
       }
       // ---- epilogue: out = O / l, lse = ln(sum of exp).  n is the same for the
       // whole CTA, so the collective loads run on every lane or none.
@@ -572,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c4 = 0; c4 < kD / 32; ++c4) {
         float o[32];
         if (n > 0) {
-          tmem_ld32(tbase + 128 + (uint32_t)c4 * 32, o);
+          tmem_ld32(obase + (uint32_t)c4 * 32, o);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0.f;

@@ -47,6 +47,9 @@ SPECS = [
     (small_spec("paged64_mha", 2, 2, 2, 128, 500, layout="paged", page_size=64, lengths="uniform:200:500"), 64),
     (small_spec("d64_gqa4", 2, 8, 2, 64, 600, lengths="uniform:1:600"), 300),
     (small_spec("d64_paged32_mha", 2, 3, 3, 64, 400, layout="paged", page_size=32, lengths="uniform:100:400"), 150),
+    # odd group size: one head per CTA, alternating S buffers; peaked scores force O rescales
+    (small_spec("gqa3_ragged", 2, 6, 2, 128, 900, lengths="uniform:1:900", q_gain=4.0), 517),
+    (small_spec("mha_d64_long", 1, 2, 2, 64, 1500, q_gain=5.0), 1500),
 ]
 
 
