@@ -64,12 +64,13 @@ def parse_args():
 # ------------------------------------------------------------------ helpers
 KERNEL_SOURCES = ("fd_split.cuh", "fd_split_mma.cuh", "fd_device.cuh", "fd_plan.h", "fd_split_launch.cuh", "fd_split_bf16.cu",
                   "fd_split_f32.cu")
+PREFILL_SOURCES = ("fd_prefill.cu", "fd_prefill.h", "fd_device.cuh")
 
 
-def source_hash() -> str:
-    """Hash of the device code of the split kernel (host-only files excluded)."""
+def source_hash(sources=KERNEL_SOURCES) -> str:
+    """Hash of a kernel's device code (host-only files excluded); the split kernel by default."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in sources:
         h.update(open(os.path.join(ROOT, "split_kv_decode_fd_gb300", "csrc", name), "rb").read())
     return h.hexdigest()[:12]
 
@@ -97,7 +98,7 @@ def measured_tensor_peak():
     return 1900.0, "fallback (1.9 PFLOP/s bf16 burst, one earlier GB300 measurement)"
 
 
-def recorded_traffic(workload_name: str):
+def recorded_traffic(workload_name: str, sources=KERNEL_SOURCES):
     """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel sources."""
     for p in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
         txt = open(p).read()
@@ -109,7 +110,7 @@ def recorded_traffic(workload_name: str):
             if ":" in line and line.startswith(("traffic_bytes_per_launch", "source_sha")):
                 k, v = line.split(":", 1)
                 vals[k.strip(" `")] = v.strip(" `")
-        if vals.get("source_sha") == source_hash() and "traffic_bytes_per_launch" in vals:
+        if vals.get("source_sha") == source_hash(sources) and "traffic_bytes_per_launch" in vals:
             try:
                 return int(float(vals["traffic_bytes_per_launch"]))
             except ValueError:
@@ -647,13 +648,14 @@ def run_prefill(args):
                    "launch": "one CUDA graph of K fd_prefill calls",
                    "kernel": "fd_prefill_kernel (tcgen05.mma M=128; q and p as bf16 hi+lo: 2 MMAs per product)"},
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
-                     "traffic": None, "peak_source": peak_src, "kernel": "fd_prefill_kernel",
+                     "traffic": recorded_traffic(spec.name, PREFILL_SOURCES), "peak_source": peak_src,
+                     "kernel": "fd_prefill_kernel",
                      "launches_per_step": 1, "mean_launch_us": ms_per_step * 1e3},
         "e2e": {"value": world * flops * k_e2e / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": q_host.numel() * 4, "d2h_bytes_per_step": (out_h.numel() + lse_h.numel()) * 4,
                 "steps": k_e2e, "api": "pinned copies + fd_prefill"},
         "gpu_launches": K, "clocks": clocks, "cpu_baseline": None, "kernel_status": fd.workspace_status(ws),
-        "source_sha": source_hash(),
+        "source_sha": source_hash(PREFILL_SOURCES),
     }
     print(json.dumps(line), flush=True)
     return 0
