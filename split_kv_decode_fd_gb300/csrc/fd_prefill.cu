@@ -118,6 +118,17 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// Ties 32 registers to the point after a tcgen05.wait::ld: an empty asm that
+// "modifies" them, so the compiler cannot move their uses above the wait.
+__device__ __forceinline__ void reg_fence32(float* v) {
+  asm volatile(""
+               : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]), "+f"(v[7]),
+                 "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]), "+f"(v[14]),
+                 "+f"(v[15]), "+f"(v[16]), "+f"(v[17]), "+f"(v[18]), "+f"(v[19]), "+f"(v[20]), "+f"(v[21]),
+                 "+f"(v[22]), "+f"(v[23]), "+f"(v[24]), "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]),
+                 "+f"(v[29]), "+f"(v[30]), "+f"(v[31]));
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -132,6 +143,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  reg_fence32(v);
 }
 
 // The same load without the wait: several may be in flight before one
@@ -159,6 +171,8 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&r)[1
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
@@ -199,6 +213,10 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
 // Byte offset of 16-byte chunk `c` (8 bf16) of row `r` in a [rows][128 B] block
 // with the 128-byte swizzle (block base 1024-aligned).
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) { return r * 128u + (((c ^ r) & 7u) << 4); }
@@ -210,9 +228,16 @@ __device__ __forceinline__ int32_t row_keys(const PrefillParams& p, int32_t L, i
   return lim < 0 ? 0 : (lim > L ? L : lim);
 }
 
-// The MMA thread's waits: false when the CTA aborts or the wait times out.
+// Waits of every role: false when the CTA aborts or the wait times out.  A
+// phase that has already completed costs one try_wait; the abort flag is read
+// only when the thread has to wait.
+__device__ __forceinline__ bool bar_ok(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_try_wait(bar, parity) || (!*abort_flag && mbar_wait(bar, parity));
+}
+
+// The MMA thread's waits, followed by the tcgen05 fence its MMAs need.
 __device__ __forceinline__ bool wait_ok(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  const bool r = !*abort_flag && mbar_wait(bar, parity);
+  const bool r = bar_ok(bar, parity, abort_flag);
   tc_fence_after();
   return r;
 }
@@ -341,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const unsigned issue = __ballot_sync(0xffffffffu, mine);
         for (int kv = 0; kv < 2; ++kv, ++u) {
           const uint32_t slot = u % kSlots, use = u / kSlots;
-          if (lane == 0 && (*abort_flag || !mbar_wait(kv_empty + slot, (use & 1) ^ 1))) ok = false;
+          if (lane == 0 && !bar_ok(kv_empty + slot, (use & 1) ^ 1, abort_flag)) ok = false;
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           if (lane == 0) mbar_arrive_expect_tx(kv_full + slot, (uint32_t)__popc(issue) * kNB * 2048u);
@@ -386,15 +411,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       // O (TMEM column o_col) += P V, P at column p_col, for the V tile in slot
-      // `slot`: 16 keys per k-step (two 8-row groups of V), P hi in the buffer's
-      // columns [0, 64), lo in [64, 128)
+      // `slot`: 16 keys per k-step (two 8-row groups of V); k-step kk's P hi is
+      // in the buffer's columns [16 kk, 16 kk + 8), its lo in the next 8
       auto issue_pv = [=](uint32_t p_col, uint32_t o_col, uint32_t slot, bool first) {
         const uint32_t v_lo = desc_lo(sbase + kSlot0 + slot * kTileBytes, kBlockBytes);
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
           for (int kk = 0; kk < kN / 16; ++kk) {
-            umma_tmem_a(tmem + o_col, tmem + p_col + (uint32_t)part * (kN / 2) + (uint32_t)kk * 8u,
+            umma_tmem_a(tmem + o_col, tmem + p_col + (uint32_t)kk * 16u + (uint32_t)part * 8u,
                         desc_of(v_lo + (uint32_t)kk * (2048u >> 4)), idO, (!first || part || kk) ? 1u : 0u);
           }
         }
@@ -502,27 +527,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t qi = it.m0 + r;
       const int32_t lim = row_keys(p, it.L, qi);
       if (n > 0) {
-        // q row, times scale*log2(e), as bf16 hi / lo in the swizzled A layout.  The
-        // previous item's S MMAs are all complete (this group saw its last S).
-        const float* qrow = p.q + (((size_t)it.b * p.Hq + h) * p.n_q + (qi < p.n_q ? qi : 0)) * kD;
-#pragma unroll 8
-        for (int c = 0; c < kD / 8; ++c) {
-          float x[8];
-          if (qi < p.n_q) {
-            const float4 a0 = __ldg(reinterpret_cast<const float4*>(qrow) + 2 * c);
-            const float4 a1 = __ldg(reinterpret_cast<const float4*>(qrow) + 2 * c + 1);
-            x[0] = a0.x; x[1] = a0.y; x[2] = a0.z; x[3] = a0.w;
-            x[4] = a1.x; x[5] = a1.y; x[6] = a1.z; x[7] = a1.w;
-          } else {
+        // q rows, times scale*log2(e), as bf16 hi / lo in the swizzled A layout.  The
+        // previous item's S MMAs are all complete (this group saw its last S).  The
+        // warp loads its 32 rows together: each load instruction covers 512
+        // contiguous bytes (128 / D rows), 8 instructions in flight per batch.
+        {
+          constexpr int kLoads = 32 * kD / 128;  // per lane, for the warp's 32 rows
+          constexpr int kBatch = kLoads < 8 ? kLoads : 8;
+          const size_t head_row0 = ((size_t)it.b * p.Hq + h) * p.n_q;
+#pragma unroll 1
+          for (int i0 = 0; i0 < kLoads; i0 += kBatch) {
+            float4 v[kBatch];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+            for (int i = 0; i < kBatch; ++i) {
+              const int e = (i0 + i) * 128 + lane * 4;  // float index within the warp's rows
+              const int32_t row = quarter * 32 + e / kD, qr = it.m0 + row;
+              v[i] = qr < p.n_q ? __ldg(reinterpret_cast<const float4*>(p.q + (head_row0 + qr) * kD + e % kD))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+              const int e = (i0 + i) * 128 + lane * 4;
+              const uint32_t row = (uint32_t)(quarter * 32 + e / kD), col = (uint32_t)(e % kD);
+              uint32_t hi0, lo0, hi1, lo1;
+              split2(v[i].x * p.qk_scale, v[i].y * p.qk_scale, hi0, lo0);
+              split2(v[i].z * p.qk_scale, v[i].w * p.qk_scale, hi1, lo1);
+              const uint32_t off = (col >> 6) * 16384u + swz(row, (col >> 3) & 7u) + ((col >> 2) & 1u) * 8u;
+              sts64(qbase + kQhi + off, hi0, hi1);
+              sts64(qbase + kQlo + off, lo0, lo1);
+            }
           }
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) split2(x[2 * e] * p.qk_scale, x[2 * e + 1] * p.qk_scale, hi[e], lo[e]);
-          const uint32_t off = (uint32_t)(c >> 3) * 16384u + swz((uint32_t)r, (uint32_t)(c & 7));
-          sts128(qbase + kQhi + off, hi[0], hi[1], hi[2], hi[3]);
-          sts128(qbase + kQlo + off, lo[0], lo[1], lo[2], lo[3]);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -536,12 +570,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t gj = g + (uint32_t)j;
         const uint32_t buf = dual ? (gj & 1) : (uint32_t)G, par = dual ? (gj >> 1) & 1 : gj & 1;
         const uint32_t tbase = tmem + buf * 256u + lane_off;  // this tile's S / P
-        if (ok && (*abort_flag || !mbar_wait(s_full + buf, par))) ok = false;
+        if (ok && !bar_ok(s_full + buf, par, abort_flag)) ok = false;
         tc_fence_after();
         float s[kN];
 #pragma unroll
         for (int c = 0; c < kN / 32; ++c) tmem_ld32_nw(tbase + (uint32_t)c * 32u, s + 32 * c);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        tmem_wait_ld();
         // mask the keys past this row's limit (only the tiles that reach it)
         const int32_t keys_left = lim - j * kN;
         if (keys_left < kN) {
@@ -559,23 +593,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha = mref == -INFINITY ? 0.f : ex2(mref - mn);
           mref = mn;
         }
-        // p = 2^(s - max), and P over this tile's S columns, 32 keys at a time:
-        // hi in [0, 64), lo in [64, 128), two keys per column.  The whole tile's
-        // S is in registers already, so the stores may overwrite any of it.
+        // p = 2^(s - max) and its bf16 hi / lo over the same columns, one k-step
+        // (16 keys) at a time: k-step kk's hi in columns 16 kk + [0, 8), its lo in
+        // 16 kk + [8, 16), two keys per column.  The whole tile's S is in
+        // registers already, so the stores may overwrite any of it.
         const float base = mref == -INFINITY ? 0.f : mref;
         float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < kN / 32; ++c) {
-          uint32_t hi[16], lo[16];
+        for (int c = 0; c < kN / 16; ++c) {
+          uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(s[32 * c + 2 * e] - base), p1 = ex2(s[32 * c + 2 * e + 1] - base);
+          for (int e = 0; e < 8; ++e) {
+            const float p0 = ex2(s[16 * c + 2 * e] - base), p1 = ex2(s[16 * c + 2 * e + 1] - base);
             sum4[(2 * e) & 3] += p0;
             sum4[(2 * e + 1) & 3] += p1;
-            split2(p0, p1, hi[e], lo[e]);
+            split2(p0, p1, w[e], w[8 + e]);
           }
-          tmem_st16u(tbase + (uint32_t)c * 16u, hi);
-          tmem_st16u(tbase + (uint32_t)(kN / 2) + (uint32_t)c * 16u, lo);
+          tmem_st16u(tbase + (uint32_t)c * 16u, w);
         }
         l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
         // Rescaling O needs the previous tile's P.V to have finished.  With two
@@ -586,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (.sync.aligned): the whole warp rescales when any of its rows must,
         // the others with alpha = 1.
         if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
-          if (dual && ok && (*abort_flag || !mbar_wait(o_done, (gj - 1) & 1))) ok = false;
+          if (dual && ok && !bar_ok(o_done, (gj - 1) & 1, abort_flag)) ok = false;
           tc_fence_after();
 #pragma unroll 1
           for (int c4 = 0; c4 < kD / 32; ++c4) {
@@ -601,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // keys past L in the last tile get p = 0, but 0 * NaN is NaN: zero those V
           // rows (head 0 does it for both: its P.V is issued first)
           const uint32_t uv = 2 * gj + 1, slot = uv % kSlots;
-          if (ok && (*abort_flag || !mbar_wait(kv_full + slot, (uv / kSlots) & 1))) ok = false;
+          if (ok && !bar_ok(kv_full + slot, (uv / kSlots) & 1, abort_flag)) ok = false;
           const int32_t nvalid = it.L - j * kN;
           const uint32_t vt = sbase + kSlot0 + slot * kTileBytes;
           const int32_t tid2 = (warp - 2) * 32 + lane;
@@ -620,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- epilogue: out = O / l, lse = ln(sum of exp).  n is the same for the
       // whole CTA, so the collective loads run on every lane or none.
       if (n > 0) {
-        if (ok && (*abort_flag || !mbar_wait(o_final + G, f & 1))) ok = false;
+        if (ok && !bar_ok(o_final + G, f & 1, abort_flag)) ok = false;
         tc_fence_after();
       }
       float* orow = p.out + (((size_t)it.b * p.Hq + h) * p.n_q + qi) * kD;
