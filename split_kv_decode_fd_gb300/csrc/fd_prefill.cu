@@ -12,7 +12,8 @@
 // the group size is odd --, tile of kPrefillRows = 128 query rows), ten warps:
 //   warp 0    TMA producer: 128-key K tiles and V tiles (16-row x 128-byte
 //             boxes, the 128-byte swizzle), each into its own slot of a ring of
-//             3 slots (6 for D = 64), shared by both heads;
+//             3 slots (6 for D = 64), shared by both heads; with one head per
+//             CTA the second head's q area adds two slots;
 //   warp 1    allocates all 512 TMEM columns and issues tcgen05.mma from one
 //             thread, per head: S = Q K^T (M=128, N=128, K=D) into the head's
 //             TMEM buffer, O += P V (M=128, N=D, K=128) into its accumulator,
@@ -68,7 +69,13 @@ struct PLayout {
   static constexpr uint32_t kSmemNeed = kBarOff + 256 + 1024;
   static constexpr uint32_t kSmemAlloc = kSmemNeed > 118784u ? kSmemNeed : 118784u;
   static_assert(D == 64 || D == 128, "head dim");
-  static_assert(kSlots <= 8, "barrier area holds 8 slots");
+  // With one head per CTA the second head's q area holds two more slots.
+  static constexpr int kSlotsOneHead = kSlots + 2;
+  static_assert(kSlotsOneHead <= 8, "barrier area holds 8 slots");
+  static_assert(2 * kTileBytes == kQGroupBytes, "two tiles fill one head's q area");
+  __device__ static uint32_t slot_off(uint32_t slot) {
+    return slot < (uint32_t)kSlots ? kSlot0 + slot * kTileBytes : kQGroupBytes + (slot - kSlots) * kTileBytes;
+  }
   static_assert(kSmemAlloc <= 232448, "shared memory");
 };
 
@@ -242,6 +249,21 @@ __device__ __forceinline__ bool wait_ok(uint64_t* bar, uint32_t parity, volatile
   return r;
 }
 
+// Position in the K/V slot ring: use u is slot u % n in phase (u / n) & 1,
+// advanced incrementally (no division on the issue path).
+struct Ring {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ Ring next(uint32_t by, uint32_t n) const {
+    Ring r = *this;
+    r.slot += by;
+    if (r.slot >= n) {
+      r.slot -= n;
+      r.phase ^= 1u;
+    }
+    return r;
+  }
+};
+
 // One work item: a tile of kM query rows of one sequence for `ngroups` heads.
 struct Item {
   int32_t b, h0, m0, kvh, L, n_tiles;
@@ -270,8 +292,9 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int32_t idx, int
 // with a CTA per item).  Every role walks the same items, and all barrier
 // phases follow two running counters of the CTA: g, the key tiles processed so
 // far, and f, the items with at least one tile so far.  Slot uses are numbered
-// u = 2 g (K) and 2 g + 1 (V): slot u % kSlots, phase u / kSlots.
-template <int D>
+// u = 2 g (K) and 2 g + 1 (V): slot u % nslots, phase u / nslots.
+// NG: query heads per CTA, 2 when the GQA group size is even, else 1.
+template <int D, int NG>
 __global__ void __launch_bounds__(kThreads, 1)
     fd_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                       const PrefillParams p) {
@@ -279,16 +302,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kD = D;
   constexpr int kNB = Lay::kNB;
   constexpr uint32_t kQhi = Lay::kQhi, kQlo = Lay::kQlo, kQGroupBytes = Lay::kQGroupBytes;
-  constexpr uint32_t kTileBytes = Lay::kTileBytes, kBlockBytes = Lay::kBlockBytes, kSlot0 = Lay::kSlot0;
+  constexpr uint32_t kBlockBytes = Lay::kBlockBytes;
   constexpr uint32_t kBarOff = Lay::kBarOff;
-  constexpr uint32_t kSlots = (uint32_t)Lay::kSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* kv_full = bars;        // [kSlots <= 8]
-  uint64_t* kv_empty = bars + 8;   // [kSlots <= 8]
+  uint64_t* kv_full = bars;        // [nslots <= 8]
+  uint64_t* kv_empty = bars + 8;   // [nslots <= 8]
   // One phase per key tile and S buffer.  Neither side can get two phases
   // ahead: S into a buffer is issued only after the P that the buffer last
   // held has arrived, and that P needed the S before it.
@@ -306,12 +328,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // at 256 G + 128.  Otherwise the second softmax group idles and the one head
   // alternates between both S buffers, tile by tile, so that S of tile j+1 is
   // computed while the softmax works on tile j.
-  const int32_t ngroups = (p.g % 2 == 0) ? 2 : 1;
+  constexpr int32_t ngroups = NG;
+  constexpr uint32_t nslots = NG == 2 ? (uint32_t)Lay::kSlots : (uint32_t)Lay::kSlotsOneHead;
   const int32_t n_m = (p.n_q + kM - 1) / kM;
   const int32_t n_items = n_m * (p.Hq / ngroups) * p.B;
 
   if (tid == 0) {
-    for (uint32_t i = 0; i < kSlots; ++i) {
+    for (uint32_t i = 0; i < nslots; ++i) {
       mbar_init(kv_full + i, 1);
       mbar_init(kv_empty + i, 1);
     }
@@ -345,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     uint32_t u = 0;  // slot uses so far
+    Ring pr;         // the next use's slot
     for (int32_t idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
       const Item it = item_of(p, idx, ngroups, n_m);
       for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
@@ -364,15 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           z = page * p.Hkv + it.kvh;
         }
         const unsigned issue = __ballot_sync(0xffffffffu, mine);
-        for (int kv = 0; kv < 2; ++kv, ++u) {
-          const uint32_t slot = u % kSlots, use = u / kSlots;
-          if (lane == 0 && !bar_ok(kv_empty + slot, (use & 1) ^ 1, abort_flag)) ok = false;
+        for (int kv = 0; kv < 2; ++kv, ++u, pr = pr.next(1, nslots)) {
+          const uint32_t slot = pr.slot;
+          if (lane == 0 && !bar_ok(kv_empty + slot, pr.phase ^ 1u, abort_flag)) ok = false;
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           if (lane == 0) mbar_arrive_expect_tx(kv_full + slot, (uint32_t)__popc(issue) * kNB * 2048u);
           __syncwarp();
           if (mine) {
-            uint8_t* dst = smem + kSlot0 + slot * kTileBytes + lane * 2048;
+            uint8_t* dst = smem + Lay::slot_off(slot) + lane * 2048;
             const CUtensorMap* map = kv == 0 ? &tmap_k : &tmap_v;
 #pragma unroll
             for (int blk = 0; blk < kNB; ++blk) tma_load_3d(dst + blk * kBlockBytes, map, kv_full + slot, blk * 64, row, z);
@@ -383,9 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) *abort_flag = 1;
     // do not leave while this warp's copies may still be landing
     if (lane == 0) {
-      const uint32_t first = u > kSlots ? u - kSlots : 0;
+      const uint32_t first = u > nslots ? u - nslots : 0;
       for (uint32_t t = first; t < u; ++t)
-        if (!mbar_wait(kv_full + t % kSlots, (t / kSlots) & 1)) atomicOr(p.err, kErrTimeout);
+        if (!mbar_wait(kv_full + t % nslots, (t / nslots) & 1)) atomicOr(p.err, kErrTimeout);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -398,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_s = [=](uint32_t d_col, int G, uint32_t slot) {
         const uint32_t d = tmem + d_col;
         const uint32_t q_lo = desc_lo(sbase + (uint32_t)G * kQGroupBytes, 0);
-        const uint32_t k_lo = desc_lo(sbase + kSlot0 + slot * kTileBytes, 0);
+        const uint32_t k_lo = desc_lo(sbase + Lay::slot_off(slot), 0);
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
@@ -414,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // `slot`: 16 keys per k-step (two 8-row groups of V); k-step kk's P hi is
       // in the buffer's columns [16 kk, 16 kk + 8), its lo in the next 8
       auto issue_pv = [=](uint32_t p_col, uint32_t o_col, uint32_t slot, bool first) {
-        const uint32_t v_lo = desc_lo(sbase + kSlot0 + slot * kTileBytes, kBlockBytes);
+        const uint32_t v_lo = desc_lo(sbase + Lay::slot_off(slot), kBlockBytes);
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
@@ -424,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
+      Ring kr;  // K of the next tile
       for (int32_t idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
         const Item it = item_of(p, idx, ngroups, n_m);
         const int32_t n = it.n_tiles;
@@ -433,14 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (ngroups == 2) {
+          Ring vprev;  // V of the previous tile
           for (int32_t j = 0; j < n; ++j) {
             const uint32_t gj = g + (uint32_t)j;
-            const uint32_t uk = 2 * gj, uv = uk + 1;
-            if (!wait_ok(kv_full + uk % kSlots, (uk / kSlots) & 1, abort_flag)) {
+            const Ring vr = kr.next(1, nslots);  // V of this tile
+            if (!wait_ok(kv_full + kr.slot, kr.phase, abort_flag)) {
               ok = false;
               break;
             }
-            issue_s(0, 0, uk % kSlots);
+            issue_s(0, 0, kr.slot);
             umma_commit(s_full + 0);
             if (j >= 1) {
               // head 1's P.V of the previous tile, then its S of this tile
@@ -448,53 +474,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
               }
-              issue_pv(256, 384, (uv - 2) % kSlots, j == 1);
-              umma_commit(kv_empty + (uv - 2) % kSlots);
+              issue_pv(256, 384, vprev.slot, j == 1);
+              umma_commit(kv_empty + vprev.slot);
             }
-            issue_s(256, 1, uk % kSlots);
+            issue_s(256, 1, kr.slot);
             umma_commit(s_full + 1);
-            umma_commit(kv_empty + uk % kSlots);
-            if (!wait_ok(kv_full + uv % kSlots, (uv / kSlots) & 1, abort_flag) ||
-                !wait_ok(p_full + 0, gj & 1, abort_flag)) {
+            umma_commit(kv_empty + kr.slot);
+            if (!wait_ok(kv_full + vr.slot, vr.phase, abort_flag) || !wait_ok(p_full + 0, gj & 1, abort_flag)) {
               ok = false;
               break;
             }
-            issue_pv(0, 128, uv % kSlots, j == 0);
+            issue_pv(0, 128, vr.slot, j == 0);
             if (j == n - 1) umma_commit(o_final + 0);
+            vprev = vr;
+            kr = kr.next(2, nslots);
           }
           if (!ok) break;
-          const uint32_t gl = g + (uint32_t)n - 1, uv = 2 * gl + 1;
-          if (!wait_ok(p_full + 1, gl & 1, abort_flag)) {
+          if (!wait_ok(p_full + 1, (g + (uint32_t)n - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
-          issue_pv(256, 384, uv % kSlots, n == 1);
-          umma_commit(kv_empty + uv % kSlots);
+          issue_pv(256, 384, vprev.slot, n == 1);
+          umma_commit(kv_empty + vprev.slot);
           umma_commit(o_final + 1);
         } else {
           // one head: S(j) into buffer j % 2, then P.V of tile j-1
+          Ring vprev;  // V of the previous tile
           for (int32_t j = 0; j <= n; ++j) {
+            const Ring vcur = kr.next(1, nslots);
             if (j < n) {
-              const uint32_t gj = g + (uint32_t)j, uk = 2 * gj;
-              if (!wait_ok(kv_full + uk % kSlots, (uk / kSlots) & 1, abort_flag)) {
+              const uint32_t gj = g + (uint32_t)j;
+              if (!wait_ok(kv_full + kr.slot, kr.phase, abort_flag)) {
                 ok = false;
                 break;
               }
-              issue_s((gj & 1) * 256u, 0, uk % kSlots);
+              issue_s((gj & 1) * 256u, 0, kr.slot);
               umma_commit(s_full + (gj & 1));
-              umma_commit(kv_empty + uk % kSlots);
+              umma_commit(kv_empty + kr.slot);
             }
             if (j >= 1) {
-              const uint32_t gp = g + (uint32_t)j - 1, uv = 2 * gp + 1;
-              if (!wait_ok(kv_full + uv % kSlots, (uv / kSlots) & 1, abort_flag) ||
+              const uint32_t gp = g + (uint32_t)j - 1;
+              if (!wait_ok(kv_full + vprev.slot, vprev.phase, abort_flag) ||
                   !wait_ok(p_full + (gp & 1), (gp >> 1) & 1, abort_flag)) {
                 ok = false;
                 break;
               }
-              issue_pv((gp & 1) * 256u, 128, uv % kSlots, j == 1);
+              issue_pv((gp & 1) * 256u, 128, vprev.slot, j == 1);
               umma_commit(o_done);
-              umma_commit(kv_empty + uv % kSlots);
+              umma_commit(kv_empty + vprev.slot);
               if (j == n) umma_commit(o_final + 0);
+            }
+            if (j < n) {
+              vprev = vcur;
+              kr = kr.next(2, nslots);
             }
           }
           if (!ok) break;
@@ -634,10 +666,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (G == 0 && j == n - 1 && it.L - j * kN < kN) {
           // keys past L in the last tile get p = 0, but 0 * NaN is NaN: zero those V
           // rows (head 0 does it for both: its P.V is issued first)
-          const uint32_t uv = 2 * gj + 1, slot = uv % kSlots;
-          if (ok && !bar_ok(kv_full + slot, (uv / kSlots) & 1, abort_flag)) ok = false;
+          const uint32_t uv = 2 * gj + 1, slot = uv % nslots;
+          if (ok && !bar_ok(kv_full + slot, (uv / nslots) & 1, abort_flag)) ok = false;
           const int32_t nvalid = it.L - j * kN;
-          const uint32_t vt = sbase + kSlot0 + slot * kTileBytes;
+          const uint32_t vt = sbase + Lay::slot_off(slot);
           const int32_t tid2 = (warp - 2) * 32 + lane;
           constexpr int kRowChunks = kD * 2 / 16;
           for (int32_t e = tid2; e < (kN - nvalid) * kRowChunks; e += 128) {
@@ -696,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, int NG>
 cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                              cudaStream_t stream) {
   static int configured = -1;
@@ -704,7 +736,7 @@ cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured != dev) {
-    e = cudaFuncSetAttribute(fd_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fd_prefill_kernel<D, NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)PLayout<D>::kSmemAlloc);
     if (e != cudaSuccess) return e;
     configured = dev;
@@ -712,11 +744,10 @@ cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const
   // One CTA per item, items numbered longest first: the hardware hands the next
   // item to whichever SM frees up (measured faster than persistent CTAs taking
   // items round-robin, whose tails do not even out).
-  const int groups = p.g % 2 == 0 ? 2 : 1;  // query heads per item
-  const int64_t items = (int64_t)((p.n_q + kM - 1) / kM) * (p.Hq / groups) * p.B;
+  const int64_t items = (int64_t)((p.n_q + kM - 1) / kM) * (p.Hq / NG) * p.B;
   if (items > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)items);
-  fd_prefill_kernel<D><<<grid, kThreads, PLayout<D>::kSmemAlloc, stream>>>(tk, tv, p);
+  fd_prefill_kernel<D, NG><<<grid, kThreads, PLayout<D>::kSmemAlloc, stream>>>(tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -724,8 +755,9 @@ cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const
 
 cudaError_t launch_prefill(int D, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                            cudaStream_t stream) {
-  if (D == 128) return launch_prefill_t<128>(tk, tv, p, stream);
-  if (D == 64) return launch_prefill_t<64>(tk, tv, p, stream);
+  const bool pair = p.g % 2 == 0;  // two query heads per CTA
+  if (D == 128) return pair ? launch_prefill_t<128, 2>(tk, tv, p, stream) : launch_prefill_t<128, 1>(tk, tv, p, stream);
+  if (D == 64) return pair ? launch_prefill_t<64, 2>(tk, tv, p, stream) : launch_prefill_t<64, 1>(tk, tv, p, stream);
   return cudaErrorInvalidValue;
 }
 
