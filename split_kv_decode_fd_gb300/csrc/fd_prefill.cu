@@ -9,7 +9,9 @@
 // query axis -- with decode.
 //
 // One CTA per (batch, pair of query heads of one GQA group -- or one head when
-// the group size is odd --, tile of kPrefillRows = 128 query rows), ten warps:
+// the group size is odd --, tile of kPrefillRows = 128 query rows), ten warps
+// (twelve with one head per CTA: warps 2 and 3 have no role there, and the
+// softmax groups are warps 4-7 and 8-11):
 //   warp 0    TMA producer: 128-key K tiles and V tiles (16-row x 128-byte
 //             boxes, the 128-byte swizzle), each into its own slot of a ring of
 //             3 slots (6 for D = 64), shared by both heads; with one head per
@@ -44,7 +46,27 @@ namespace {
 
 constexpr int kM = kPrefillRows;   // query rows per CTA (TMEM lanes)
 constexpr int kN = kPrefillKeys;   // keys per tile
-constexpr int kThreads = 320;      // producer, MMA, two softmax groups of four warps
+// Threads: producer and MMA warps, then two softmax groups of four warps from
+// warp kSoftmax0.  With one head per CTA two idle warps complete the first
+// warpgroup, which setmaxnreg needs (measured: the two-head variant runs ~2 %
+// faster without them).
+template <int NG>
+constexpr int kSoftmax0 = NG == 2 ? 2 : 4;
+template <int NG>
+constexpr int kThreads = (kSoftmax0<NG> + 8) * 32;
+// Registers: the launch gives every thread kLaunchRegs (65536 / 384, rounded
+// down to 8).  With one head per CTA the first warpgroup then gives registers
+// back (setmaxnreg.dec) and the softmax warpgroups take them (setmaxnreg.inc),
+// so that a thread holds a tile's 128 scores without spilling (measured +5 %
+// there; with two heads per CTA the issuing thread's code is the one that
+// matters, and it keeps the launch count).  An increase waits until the CTA's
+// pool has the registers, so the split must add up exactly; the host launches
+// that variant only when the compiled kernel has kLaunchRegs registers.
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsLow = 88;
+constexpr int kRegsHigh = 208;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads<1> * kLaunchRegs, "register split exceeds the pool");
+static_assert(kRegsLow + 2 * kRegsHigh <= 512, "one warp of each group per sub-partition: 16384 registers");
 constexpr float kTau = 8.0f;
 constexpr float kLn2f = 0.6931471805599453f;
 constexpr uint32_t kTmemCols = 512;  // per head (256 each): S / P at +0, O (D columns) at +128
@@ -200,6 +222,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Register count of the calling warp's role (one head per CTA only).
+template <int NG, uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  if constexpr (NG == 1) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int NG, uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  if constexpr (NG == 1) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // 2^x on the special-function unit (inputs here are <= 0 or -inf).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -295,7 +327,7 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int32_t idx, int
 // u = 2 g (K) and 2 g + 1 (V): slot u % nslots, phase u / nslots.
 // NG: query heads per CTA, 2 when the GQA group size is even, else 1.
 template <int D, int NG>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads<NG>, 1)
     fd_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                       const PrefillParams p) {
   using Lay = PLayout<D>;
@@ -365,8 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
 
+  // Each role sets its register count first thing, so that the compiler
+  // allocates the role's code for that count.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    regs_dec<NG, kRegsLow>();
     uint32_t u = 0;  // slot uses so far
     Ring pr;         // the next use's slot
     for (int32_t idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
@@ -413,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
+    regs_dec<NG, kRegsLow>();
     if (lane == 0) {
       constexpr uint32_t idS = instr_desc(kM, kN, false);
       constexpr uint32_t idO = instr_desc(kM, kD, true);
@@ -542,9 +578,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(drain);
       if (!mbar_wait(drain, 0)) atomicOr(p.err, kErrTimeout);
     }
-  } else if ((warp - 2) / 4 < ngroups) {
+  } else if (warp < kSoftmax0<NG>) {
+    regs_dec<NG, kRegsLow>();  // no role
+  } else if ((warp - kSoftmax0<NG>) / 4 >= ngroups) {
+    regs_inc<NG, kRegsHigh>();  // the second softmax group, idle with one head per CTA
+  } else {
     // ------------------------------------------------------------ softmax, head G
-    const int32_t G = (warp - 2) / 4;
+    regs_inc<NG, kRegsHigh>();
+    const int32_t G = (warp - kSoftmax0<NG>) / 4;
     const int32_t quarter = warp & 3;
     const int32_t r = quarter * 32 + lane;  // query row in the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -670,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok && !bar_ok(kv_full + slot, (uv / nslots) & 1, abort_flag)) ok = false;
           const int32_t nvalid = it.L - j * kN;
           const uint32_t vt = sbase + Lay::slot_off(slot);
-          const int32_t tid2 = (warp - 2) * 32 + lane;
+          const int32_t tid2 = (warp - kSoftmax0<NG>) * 32 + lane;
           constexpr int kRowChunks = kD * 2 / 16;
           for (int32_t e = tid2; e < (kN - nvalid) * kRowChunks; e += 128) {
             const uint32_t row = (uint32_t)(nvalid + e / kRowChunks), c = (uint32_t)(e % kRowChunks);
@@ -736,6 +777,11 @@ cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured != dev) {
+    // the setmaxnreg split assumes this launch register count: refuse any other
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fd_prefill_kernel<D, NG>);
+    if (e != cudaSuccess) return e;
+    if (NG == 1 && fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(fd_prefill_kernel<D, NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)PLayout<D>::kSmemAlloc);
     if (e != cudaSuccess) return e;
@@ -747,7 +793,7 @@ cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const
   const int64_t items = (int64_t)((p.n_q + kM - 1) / kM) * (p.Hq / NG) * p.B;
   if (items > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)items);
-  fd_prefill_kernel<D, NG><<<grid, kThreads, PLayout<D>::kSmemAlloc, stream>>>(tk, tv, p);
+  fd_prefill_kernel<D, NG><<<grid, kThreads<NG>, PLayout<D>::kSmemAlloc, stream>>>(tk, tv, p);
   return cudaGetLastError();
 }
 
