@@ -211,6 +211,9 @@ FD_API fd_status fd_append_decode(const float* q, const void* k_new, const void*
  *   workspace: at least 256 bytes, zero-filled once (its first word is the
  *   kernels' error word, read by fd_workspace_status).  out, lse as in
  *   fd_decode_rows.  One launch, asynchronous on `stream`.
+ *   FD_ERR_CUDA, with nothing launched, also when the kernel variant for an odd
+ *   group size (one query head per CTA, which redistributes registers between
+ *   its warps) was not compiled with the register count it assumes.
  */
 FD_API fd_status fd_prefill(const float* q, int32_t n_q, int32_t causal, const fd_kv_desc* kv, float* out,
                             float* lse, int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_lens,
