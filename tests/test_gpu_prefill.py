@@ -158,3 +158,21 @@ def test_prefill_repeats_bit_identically():
         o, l = run_prefill(case, q, True)
         torch.cuda.synchronize()
         assert torch.equal(o, first[0]) and torch.equal(l, first[1])
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (6, 2)], ids=["two_heads_per_cta", "one_head_per_cta"])
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+def test_prefill_sequences_without_keys(hq, hkv, layout):
+    """Sequences with L_b = 0 between ones with keys: their items have no key tiles
+    (out = 0, lse = -inf), and the CTAs' barrier phases stay in step around them."""
+    spec = small_spec("zero_len", 5, hq, hkv, 128, 400, layout=layout, page_size=16)
+    case = make_case(spec, "cuda", lengths=[0, 300, 0, 1, 400])
+    q = window_q(case, 140, seed=12)
+    for causal in (True, False):
+        out, lse = run_prefill(case, q, causal)
+        ref_out, ref_lse = oracle_rows(case, q, causal)
+        torch.cuda.synchronize()
+        assert_close(np64(out), ref_out, "out")
+        assert_close(np64(lse), ref_lse, "lse")
+        assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
+        assert torch.all(torch.isneginf(lse[0])) and torch.all(torch.isneginf(lse[2]))
