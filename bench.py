@@ -109,7 +109,8 @@ def recorded_traffic(workload_name: str, sources=KERNEL_SOURCES):
             line = line.strip().lstrip("-* ").strip()
             if ":" in line and line.startswith(("traffic_bytes_per_launch", "source_sha")):
                 k, v = line.split(":", 1)
-                vals[k.strip(" `")] = v.strip(" `")
+                v = v.strip(" `").split()
+                vals[k.strip(" `")] = v[0].strip("`") if v else ""
         if vals.get("source_sha") == source_hash(sources) and "traffic_bytes_per_launch" in vals:
             try:
                 return int(float(vals["traffic_bytes_per_launch"]))
