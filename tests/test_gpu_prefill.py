@@ -94,9 +94,11 @@ def test_prefill_padding_is_bit_exact(layout):
         assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_prefill_long_prompt_sampled():
-    """A 4096-token causal prompt over a 4096-key cache (B=1, Hq=32, Hkv=8): sampled rows."""
-    spec = small_spec("prompt4k", 1, 32, 8, 128, 4096)
+@pytest.mark.parametrize("hkv", [8, 32], ids=["gqa4", "mha"])
+def test_prefill_long_prompt_sampled(hkv):
+    """A 4096-token causal prompt over a 4096-key cache (B=1, Hq=32; the benchmark's shape, GQA
+    and MHA, i.e. both kernel variants): sampled rows."""
+    spec = small_spec("prompt4k", 1, 32, hkv, 128, 4096)
     case = make_case(spec, "cuda")
     n_q = 4096
     q = window_q(case, n_q, seed=11)
@@ -105,7 +107,7 @@ def test_prefill_long_prompt_sampled():
     assert torch.isfinite(out).all()
     r = np.random.default_rng(0)
     rows = [(int(r.integers(0, 32)), int(r.integers(0, n_q))) for _ in range(12)] + [(0, 0), (31, n_q - 1)]
-    g = 4
+    g = 32 // hkv
     for h, i in rows:
         lim = oracle.row_key_limit(4096, n_q, i, True)
         kvh = oracle.kv_head_for(h, g)
