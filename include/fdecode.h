@@ -30,7 +30,9 @@
  *
  * General rules for every call:
  *   - Pointers are DEVICE pointers unless the name ends in _host.
- *   - All memory is owned by the caller; the library allocates nothing.
+ *   - All memory is owned by the caller; the library allocates nothing.  The
+ *     one exception is the fixed FD_STATIC_SCRATCH_BYTES device array that
+ *     fd_decode_static uses in place of a workspace (see there).
  *   - Calls enqueue work on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and return without waiting, except fd_decode_host and
  *     fd_workspace_status, which synchronise the stream.
@@ -290,9 +292,9 @@ FD_API fd_status fd_decode_host(const float* q_host, const fd_kv_desc* kv, float
  *   merge counters, split partials) is one file-scope device array of
  *   FD_STATIC_SCRATCH_BYTES inside the library; every GPU that loads the
  *   library holds it until the process exits.
- *   The first call on a device looks the array's device address up
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
+ *   Every call looks the array's device address up on the current device
+ *   (cudaGetSymbolAddress); the first call on a device also loads the
+ *   library's module there, so make that first call before any stream capture.
  *   Returns FD_ERR_WORKSPACE_TOO_SMALL, before any launch, when the problem
  *   needs more scratch than the array holds (fd_workspace_bytes of the same
  *   problem, minus its host-staging part, is the amount needed).
@@ -301,12 +303,25 @@ FD_API fd_status fd_decode_host(const float* q_host, const fd_kv_desc* kv, float
  *   All calls share the one array, and it keeps the last call's contents:
  *   calls that overlap on the GPU (different streams, other host threads)
  *   race on it and must be ordered by the caller.
+ *   Kernel-side errors (a block-table entry outside the pool, a wait that
+ *   gave up) are recorded in the array's error word: read them with
+ *   fd_static_status after the call and before the next fd_decode_static
+ *   call on that device, which clears the word.
  */
 #define FD_STATIC_SCRATCH_BYTES (16u << 20)
 
 FD_API fd_status fd_decode_static(const float* q, const fd_kv_desc* kv, float* out, float* lse, int32_t B,
                                   int32_t Hq, int32_t Hkv, const int32_t* seq_lens, int32_t max_seq_len,
                                   int32_t D, float scale, int32_t n_splits, void* stream);
+
+/*
+ * fd_workspace_status for fd_decode_static: synchronise `stream`, then report
+ * (and clear) the error word in the library's static scratch array on the
+ * current device -- FD_OK, FD_ERR_BAD_INDEX or FD_ERR_TIMEOUT, raised by the
+ * kernels of the most recent fd_decode_static call there.  Like that call it
+ * has no counterpart on the pages and allocates nothing.
+ */
+FD_API fd_status fd_static_status(void* stream);
 
 /*
  * Host-side description of the work decomposition, for inspection and tests
@@ -324,6 +339,22 @@ FD_API fd_status fd_decode_static(const float* q, const fd_kv_desc* kv, float* o
 FD_API int64_t fd_plan_pieces(int32_t B, int32_t Hq, int32_t Hkv, int32_t kv_dtype, const int32_t* seq_lens_host,
                               int32_t max_seq_len, int32_t n_splits, int32_t grid, int32_t* pieces,
                               int64_t capacity);
+
+/*
+ * Testing hook for the kernels' bounded waits; off by default.  Every
+ * mbarrier wait of the split kernel gives up after a time limit (2 s by
+ * default), records FD_ERR_TIMEOUT in the error word, lets the copies it
+ * issued land and exits, so the context stays usable.  With stage >= 0, the
+ * split kernels launched afterwards (fd_decode and every call built on it,
+ * fd_split_partial) skip the copies of stage number `stage` in their first
+ * CTA, so the wait for that stage runs out; wait_limit_ns > 0 shortens every
+ * wait of those kernels to that many nanoseconds (0 keeps the default).  The
+ * call's output is then undefined and fd_workspace_status (or
+ * fd_static_status) reports FD_ERR_TIMEOUT; the workspace stays valid for the
+ * next call.  stage < 0 switches the hook off and restores the default limit.
+ * A process-wide setting, read when a call is made.
+ */
+FD_API void fd_debug_stall(int32_t stage, int64_t wait_limit_ns);
 
 /* Static description of a status code. */
 FD_API const char* fd_status_string(fd_status status);

@@ -19,6 +19,7 @@ from .fdecode import (  # noqa: F401
     attend,
     attend_backend,
     decode_static,
+    static_status,
     library_path,
     load_library,
     plan_pieces,

@@ -50,8 +50,9 @@ def exchange_partials(o_part, m_part, l_part, group=None):
     Inputs: ``o_part [B, Hq, 1, D]``, ``m_part`` and ``l_part [B, Hq, 1]`` (the
     ``fd_split_partial`` layout with one split).  Outputs: ``[B, Hq, world, D]``
     and ``[B, Hq, world]``.  One collective: the three are packed into
-    ``[B, Hq, D + 2]`` first.  Works on any backend whose tensors live where
-    the process group expects them (NCCL: CUDA tensors; gloo: CPU tensors).
+    ``[B, Hq, D + 2]`` first.  NCCL gathers the CUDA tensors directly; a gloo
+    group gathers host tensors, so CUDA inputs are staged through host memory
+    there and the result is moved back to the inputs' device.
     """
     import torch
     import torch.distributed as dist
@@ -61,9 +62,12 @@ def exchange_partials(o_part, m_part, l_part, group=None):
     B, Hq, _, D = o_part.shape
     packed = torch.cat([o_part[:, :, 0, :], m_part[:, :, :1], l_part[:, :, :1]], dim=-1).contiguous()
     world = dist.get_world_size(group)
+    device = packed.device
+    if packed.is_cuda and dist.get_backend(group) == "gloo":
+        packed = packed.cpu()
     parts = [torch.empty_like(packed) for _ in range(world)]
     dist.all_gather(parts, packed, group=group)
-    allp = torch.stack(parts, dim=2)  # [B, Hq, world, D + 2]
+    allp = torch.stack(parts, dim=2).to(device)  # [B, Hq, world, D + 2]
     return allp[..., :D].contiguous(), allp[..., D].contiguous(), allp[..., D + 1].contiguous()
 
 

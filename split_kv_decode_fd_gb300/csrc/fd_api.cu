@@ -198,6 +198,10 @@ fd_status make_maps(const fd_kv_desc* kv, int B, int Hkv, int D, CUtensorMap* tk
   return FD_OK;
 }
 
+// Testing hook of the bounded waits (fd_debug_stall): off by default.
+std::atomic<int32_t> g_stall_it{-1};
+std::atomic<int64_t> g_wait_ns{0};
+
 SplitParams base_params(const float* q, const fd_kv_desc* kv, int B, int Hq, int Hkv,
                         const int32_t* seq_lens, int max_seq_len, float scale) {
   SplitParams p;
@@ -221,6 +225,8 @@ SplitParams base_params(const float* q, const fd_kv_desc* kv, int B, int Hq, int
   p.qk_scale = (float)((double)scale * 1.4426950408889634);
   p.n_q = 1;
   p.causal = 0;
+  p.stall_it = g_stall_it.load(std::memory_order_relaxed);
+  p.wait_ns = (uint64_t)g_wait_ns.load(std::memory_order_relaxed);
   return p;
 }
 
@@ -270,6 +276,11 @@ const char* fd_status_string(fd_status s) {
 }
 
 int32_t fd_version(void) { return 100; }
+
+void fd_debug_stall(int32_t stage, int64_t wait_limit_ns) {
+  g_wait_ns.store(stage >= 0 && wait_limit_ns > 0 ? wait_limit_ns : 0, std::memory_order_relaxed);
+  g_stall_it.store(stage >= 0 ? stage : -1, std::memory_order_relaxed);
+}
 
 int32_t fd_split_size(int32_t max_seq_len, int32_t n_splits) {
   return explicit_split_size(max_seq_len, n_splits);
@@ -638,21 +649,15 @@ static_assert(kStaticScratchBytes % 256 == 0, "scratch size must keep 256-byte a
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-// Device address of g_static_scratch on each device, looked up once per device
-// (the host-side symbol is only a stand-in and must never reach a kernel).
-std::mutex g_static_mutex;
-void* g_static_ptr[64] = {};
-
+// Device address of g_static_scratch on the current device.  The host-side
+// symbol is only a stand-in and must never reach a kernel; the address is
+// looked up on every call (cheap once the library's module is loaded on the
+// device), so a context that was torn down and created again is never handed
+// a stale address.
 fd_status static_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FD_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_static_mutex);
-  if (!g_static_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return FD_ERR_CUDA;
-    g_static_ptr[dev] = p;
-  }
-  *out = g_static_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return FD_ERR_CUDA;
+  *out = p;
   return FD_OK;
 }
 
@@ -707,4 +712,13 @@ extern "C" fd_status fd_decode_static(const float* q, const fd_kv_desc* kv, floa
   if ((st = launch(kv, D, p, grid, s)) != FD_OK) return st;
   const cudaError_t e = launch_combine(D, p.o_part, p.m_part, p.l_part, out, lse, B * Hq, n_splits, s);
   return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+extern "C" fd_status fd_static_status(void* stream) {
+  void* base = nullptr;
+  fd_status st = static_scratch(&base);
+  if (st != FD_OK) return st;
+  // the error word sits at the start of the array, where fd_decode_static puts
+  // the workspace header
+  return fd_workspace_status(base, kHeaderBytes, stream);
 }

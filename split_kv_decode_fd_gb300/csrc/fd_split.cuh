@@ -75,7 +75,16 @@ struct SplitParams {
   void* k_cache;           // the cache's K and V base pointers (pool when paged)
   void* v_cache;
   int64_t capacity;        // contiguous: rows per (b, KV head)
+  // Bounded waits: every mbarrier wait gives up after wait_ns (0 = kWaitLimitNs).
+  // Testing hook: stall_it >= 0 makes the producer of CTA 0 skip the copies of
+  // its stage number stall_it, so that the consumers' wait on it runs out.
+  uint64_t wait_ns;
+  int32_t stall_it;
 };
+
+__device__ __forceinline__ unsigned long long wait_limit(const SplitParams& p) {
+  return p.wait_ns ? (unsigned long long)p.wait_ns : kWaitLimitNs;
+}
 
 // Keys seen by the heads of one piece: head0 + j for j < nh; virtual head
 // h' = head * n_q + row sees keys t < len - (n_q - 1 - row) when causal.
@@ -361,6 +370,7 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
   uint64_t* qfull = empty + C::kStages;
   uint64_t* qempty = qfull + 2;
   uint32_t it = 0, qi = 0;
+  uint32_t stalled = 0xffffffffu;  // stage skipped by the testing hook
   bool ok = true;
   Groups gr;
   gr.g = p.g;
@@ -383,7 +393,7 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
     const int32_t kvh = kv_head_of_vkv(gr, pc.vkv);
     if (lane == 0) {
       const uint32_t slot = qi % C::kQBufs;
-      if (!mbar_wait(qempty + slot, ((qi / C::kQBufs) & 1) ^ 1)) ok = false;
+      if (!mbar_wait_for(qempty + slot, ((qi / C::kQBufs) & 1) ^ 1, wait_limit(p))) ok = false;
       if (ok) {
         const uint32_t bytes = (uint32_t)nh * C::D * 4;
         mbar_arrive_expect_tx(qfull + slot, bytes);
@@ -444,16 +454,18 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
         const unsigned issue = __ballot_sync(0xffffffffu, mine);
         const uint32_t stage = it % C::kStages;
         const uint32_t phase = (it / C::kStages) & 1;
+        const bool stall = p.stall_it >= 0 && it == (uint32_t)p.stall_it && blockIdx.x == 0 && blockIdx.y == 0;
         if (lane == 0) {
-          if (*abort_flag || !mbar_wait(empty + stage, phase ^ 1)) {
+          if (*abort_flag || !mbar_wait_for(empty + stage, phase ^ 1, wait_limit(p))) {
             ok = false;
-          } else {
+          } else if (!stall) {
             mbar_arrive_expect_tx(full + stage, (uint32_t)__popc(issue) * C::kNB * 2 * C::kBoxBytes);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        if (mine) {
+        if (stall) stalled = it;  // nothing issued: this stage never completes
+        if (mine && !stall) {
           uint8_t* kdst = smem + stage * C::kStageBytes + lane * C::kBoxBytes;
           uint8_t* vdst = kdst + C::kTileBytes;
           // paged pool viewed as [num_pages * Hkv, page_size, D]; contiguous [B * Hkv, T_cap, D]
@@ -479,7 +491,8 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
   if (lane == 0) {
     const uint32_t n = it < (uint32_t)C::kStages ? it : (uint32_t)C::kStages;
     for (uint32_t j = it - n; j < it; ++j) {
-      if (!mbar_wait(full + (j % C::kStages), (j / C::kStages) & 1)) raise_error(p.err, kErrTimeout);
+      if (j == stalled) continue;
+      if (!mbar_wait_for(full + (j % C::kStages), (j / C::kStages) & 1, wait_limit(p))) raise_error(p.err, kErrTimeout);
     }
   }
 }
@@ -800,7 +813,7 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
     if (app && warp == (app_r >> 5))
       arow.prefetch(p, pc.b, kv_head_of_vkv(gr, pc.vkv), pc.len - 1, lane, pc.vkv % gr.nsub == 0);
     if (nonempty && ok) {
-      if (!mbar_wait(qfull + qslot, (qi / C::kQBufs) & 1)) {
+      if (!mbar_wait_for(qfull + qslot, (qi / C::kQBufs) & 1, wait_limit(p))) {
         ok = false;
         *abort_flag = 1;
       }
@@ -814,7 +827,7 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
       }
       for (int32_t t0 = pc.tok_begin; ok && t0 < pc.tok_end; t0 += C::kBT, ++it) {
         const uint32_t stage = it % C::kStages;
-        if (*abort_flag || !mbar_wait(full + stage, (it / C::kStages) & 1)) {
+        if (*abort_flag || !mbar_wait_for(full + stage, (it / C::kStages) & 1, wait_limit(p))) {
           ok = false;
           *abort_flag = 1;
           break;

@@ -17,7 +17,7 @@ import numpy as np
 
 __all__ = [
     "FdError", "KvDesc", "library_path", "load_library", "workspace_bytes", "split_size", "plan_pieces",
-    "Workspace", "decode", "decode_rows", "append_decode", "prefill", "attend", "attend_backend", "decode_host", "decode_static", "split_partial", "combine", "workspace_status",
+    "Workspace", "decode", "decode_rows", "append_decode", "prefill", "attend", "attend_backend", "decode_host", "decode_static", "static_status", "split_partial", "combine", "workspace_status",
 ]
 
 FD_OK, FD_ERR_INVALID_ARG, FD_ERR_UNSUPPORTED, FD_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3
@@ -85,6 +85,7 @@ def load_library(path: Optional[str] = None):
             "fd_plan_pieces": (c_i64, [c_i32, c_i32, c_i32, c_i32, vp, c_i32, c_i32, c_i32, vp, c_i64]),
             "fd_decode_static": (ctypes.c_int, [vp, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32, c_i32, f32,
                                                 c_i32, vp]),
+            "fd_static_status": (ctypes.c_int, [vp]),
             "fd_decode_rows": (ctypes.c_int, [vp, c_i32, c_i32, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32,
                                               c_i32, f32, c_i32, vp, c_sz, vp]),
             "fd_append_decode": (ctypes.c_int, [vp, vp, vp, kvp, vp, vp, c_i32, c_i32, c_i32, vp, c_i32, c_i32, f32,
@@ -97,6 +98,7 @@ def load_library(path: Optional[str] = None):
             "fd_backend_name": (ctypes.c_char_p, [c_i32]),
             "fd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "fd_version": (c_i32, []),
+            "fd_debug_stall": (None, [c_i32, c_i64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -421,6 +423,14 @@ def decode_static(q, k, v, *, out, lse=None, seq_lens=None, max_seq_len=None, bl
                                  float(scale), int(n_splits), _stream_handle(q.device, stream))
     _check(st, "fd_decode_static")
     return out, lse
+
+
+def static_status(device=None, stream=None) -> int:
+    """``fd_static_status``: synchronise and return (then clear) the error word of the
+    static scratch array that ``decode_static`` uses (0 = no error)."""
+    torch = _torch()
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    return int(_lib().fd_static_status(_stream_handle(device, stream)))
 
 
 def decode_host(q_host, k, v, *, seq_lens_host=None, max_seq_len=None, block_table=None, scale=None,

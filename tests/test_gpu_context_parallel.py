@@ -3,7 +3,11 @@
 Ranks are emulated one after another on the one GPU (their kernels never wait on
 each other): each computes its slice's partial state with ``fd_split_partial``, the
 states are concatenated in rank order as ``exchange_partials`` lays them out, and
-``fd_combine`` merges them.  A one-rank NCCL group runs the full ``cp_decode`` path.
+``fd_combine`` merges them.  A one-rank NCCL group runs the full ``cp_decode`` path,
+and two or three processes sharing the one GPU run it over a gloo group: each
+process holds its own slice of the cache, runs the kernels on it, exchanges the
+partial states through host memory and merges them, so the processes' kernels are
+independent and only the host exchange connects them.
 """
 
 import os
@@ -72,10 +76,10 @@ def test_emulated_ranks_128k():
         parts.append(fd.split_partial(case.q, k, v, 1, max_seq_len=hi - lo, scale=case.spec.scale))
     out, lse = fd.combine(torch.cat([p[0] for p in parts], 2), torch.cat([p[1] for p in parts], 2),
                           torch.cat([p[2] for p in parts], 2))
-    full_out, full_lse = fd.decode(case.q, case.k, case.v, scale=case.spec.scale)
     torch.cuda.synchronize()
-    assert_close(np64(out), np64(full_out).astype(np.float64), "out vs single-GPU decode")
-    assert_close(np64(lse), np64(full_lse).astype(np.float64), "lse vs single-GPU decode")
+    ref_out, ref_lse = oracle_for(case)
+    assert_close(np64(out), ref_out, "out")
+    assert_close(np64(lse), ref_lse, "lse")
 
 
 def _nccl_one_rank(port, errq):
@@ -111,3 +115,42 @@ def test_cp_decode_through_a_one_rank_nccl_group():
         errors.append(errq.get())
     assert not errors, errors
     assert p.exitcode == 0
+
+
+def _gloo_rank(rank, world, port, spec, errq):
+    try:
+        from split_kv_decode_fd_gb300.context_parallel import cp_decode
+        os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), NCCL_NVLS_ENABLE="0")
+        torch.cuda.set_device(0)
+        torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+        case = make_case(spec, "cuda")  # the same seeded inputs in every process
+        k, v, n, cap = local_cache(case, world, rank)
+        out, lse = cp_decode(case.q, k, v, seq_lens_local=n, max_local_len=cap, scale=spec.scale)
+        torch.cuda.synchronize()
+        ref_out, ref_lse = oracle_for(case)
+        assert_close(np64(out), ref_out, f"rank {rank} out")
+        assert_close(np64(lse), ref_lse, f"rank {rank} lse")
+        torch.distributed.destroy_process_group()
+    except Exception as e:  # noqa: BLE001
+        errq.put(f"rank {rank}: {type(e).__name__}: {e}")
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_cp_decode_across_processes_over_gloo(world):
+    """cp_decode in `world` processes on the one GPU: kernels per rank, exchange over gloo, merge."""
+    spec = small_spec("cp_gloo", 3, 16, 4, 128, 2000, lengths="uniform:1:2000", seed=91)
+    ctx = mp.get_context("spawn")
+    errq = ctx.SimpleQueue()
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    procs = [ctx.Process(target=_gloo_rank, args=(r, world, port, spec, errq)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(300)
+    errors = []
+    while not errq.empty():
+        errors.append(errq.get())
+    assert not errors, errors
+    assert all(p.exitcode == 0 for p in procs)
