@@ -95,13 +95,21 @@ FD_HD int32_t balanced_ctas(int64_t total, int32_t launched) {
   return total < (int64_t)launched ? (int32_t)total : launched;
 }
 
+// Exact floor(n / d) for 0 <= n, 0 < d; 32-bit division whenever both fit
+// (a 64-bit division is a long instruction sequence on the GPU, and the plan
+// is walked at the start of every CTA and of every piece).
+FD_HD int64_t div_floor(int64_t n, int64_t d) {
+  if (n <= 0xffffffffLL && d <= 0xffffffffLL) return (int64_t)((uint32_t)n / (uint32_t)d);
+  return n / d;
+}
+
 // Balanced plan: CTA range bounds and the CTA owning a flat tile.
 FD_HD int64_t range_begin(int64_t total, int32_t grid, int32_t cta) {
-  return (total * (int64_t)cta) / (int64_t)grid;
+  return div_floor(total * (int64_t)cta, (int64_t)grid);
 }
 
 FD_HD int32_t cta_of_tile(int64_t total, int32_t grid, int64_t tile) {
-  return (int32_t)(((tile + 1) * (int64_t)grid - 1) / total);
+  return (int32_t)div_floor((tile + 1) * (int64_t)grid - 1, total);
 }
 
 // One unit of work: a run of consecutive keys of one (b, virtual kv head).
@@ -141,8 +149,8 @@ struct BalancedWalk {
     b = lo;
     while (tl.tiles(b) == 0) ++b;  // empty sequences own no tiles
     int64_t off = flat - (int64_t)hv * tl.prefix(b);
-    vkv = (int32_t)(off / tl.tiles(b));
-    tile = (int32_t)(off % tl.tiles(b));
+    vkv = (int32_t)div_floor(off, tl.tiles(b));
+    tile = (int32_t)(off - (int64_t)vkv * tl.tiles(b));
   }
 
   FD_HD bool done() const { return flat >= end; }

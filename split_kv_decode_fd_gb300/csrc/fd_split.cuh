@@ -379,15 +379,24 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
   gr.hv = p.hv;
 
   constexpr int kPageAhead = 4;
+  // Contiguous caches: K/V are read once, so their L2 lines go first (measured
+  // faster).  The paged pool keeps the default policy (evict-first measured ~1 %
+  // slower there).
+  const uint64_t stream_policy = policy_evict_first();
   // one tile advances a lane's position by step_q pages and step_r rows
   const int32_t step_q = p.paged ? C::kBT / p.page_size : 0;
   const int32_t step_r = p.paged ? C::kBT % p.page_size : 0;
 
   PieceIter pieces(p, tl, total);
   Piece pc;
+  bool waited = false;
   while (pieces.next(pc)) {
     if (!ok) break;
     if (pc.tok_end <= pc.tok_begin) continue;
+    if (!waited) {  // first memory access of this warp: q, the block table, K/V
+      pdl_wait();
+      waited = true;
+    }
     int32_t head0, nh;
     vkv_heads(gr, pc.vkv, &head0, &nh);
     const int32_t kvh = kv_head_of_vkv(gr, pc.vkv);
@@ -474,8 +483,13 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
           for (int nb = 0; nb < C::kNB; ++nb) {
             const int32_t x = nb * (128 / C::kEs);
             const int32_t off = nb * C::kBT * 128;
-            tma_load_3d(kdst + off, tk, full + stage, x, row, z);
-            tma_load_3d(vdst + off, tv, full + stage, x, row, z);
+            if (p.paged) {
+              tma_load_3d(kdst + off, tk, full + stage, x, row, z);
+              tma_load_3d(vdst + off, tv, full + stage, x, row, z);
+            } else {
+              tma_load_3d_hint(kdst + off, tk, full + stage, x, row, z, stream_policy);
+              tma_load_3d_hint(vdst + off, tv, full + stage, x, row, z, stream_policy);
+            }
           }
         }
         t0 += C::kBT;
@@ -782,6 +796,7 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
   gr.nsub = p.nsub;
   gr.hv = p.hv;
 
+  pdl_wait();  // before the first write (outputs, partials, counters, the cache)
   // Balanced plan: sequences with no keys own no tile; CTA b % grid writes their outputs.
   if (balanced && fused) {
     for (int32_t b = blockIdx.x; b < p.B; b += gridDim.x) {
@@ -803,6 +818,21 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
     int32_t head0, nh;
     vkv_heads(gr, pc.vkv, &head0, &nh);
     const bool nonempty = pc.tok_end > pc.tok_begin;
+    // Does this piece hold the whole sequence?  Then it is the output.  (Worked
+    // out here, while the piece's first tile is still on its way, rather than
+    // after its last tile, where it would delay the merge.)
+    int npieces = 1;
+    int32_t first = 0;  // balanced: first CTA holding this sequence
+    const int32_t pair = pc.b * p.hv + pc.vkv;
+    if (balanced) {
+      int32_t last;
+      balanced_pair_ctas(tl, p.hv, total, balanced_ctas(total, (int32_t)gridDim.x), pc.b, pc.vkv, &first,
+                         &last);
+      npieces = last - first + 1;
+    } else {
+      npieces = p.n_splits;
+    }
+    const bool final_here = fused && npieces == 1;
     eng.reset();
     const uint32_t qslot = qi % C::kQBufs;
     // Fused append: the warp owning the new token's row prefetches it now.
@@ -851,20 +881,6 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
       if (nonempty && tid == 0) mbar_arrive(qempty + qslot);
     }
     if (nonempty) ++qi;
-
-    // Does this piece hold the whole sequence?  Then it is the output.
-    int npieces = 1;
-    int32_t first = 0;  // balanced: first CTA holding this sequence
-    const int32_t pair = pc.b * p.hv + pc.vkv;
-    if (balanced) {
-      int32_t last;
-      balanced_pair_ctas(tl, p.hv, total, balanced_ctas(total, (int32_t)gridDim.x), pc.b, pc.vkv, &first,
-                         &last);
-      npieces = last - first + 1;
-    } else {
-      npieces = p.n_splits;
-    }
-    const bool final_here = fused && npieces == 1;
 
     // kPubHeads heads per round; rounds > 1 only with sixteen heads per CTA
     constexpr int PH = C::kPubHeads;
@@ -1000,6 +1016,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   for (int i = tid; i < C::kQBufs * C::G * C::D; i += C::kThreads)
     reinterpret_cast<float*>(smem + C::kQOff)[i] = 0.f;
 
+  // Let the next kernel on the stream be scheduled as SMs free up.  Nothing
+  // above touched global memory; with no lengths to read, the plan needs none
+  // either, and each warp waits for the kernel before it (pdl_wait) only at
+  // its first access, so the producer walks its plan meanwhile.
+  pdl_launch_dependents();
+  if (p.seq_lens != nullptr) pdl_wait();
   CtaTiles tl;
   tl.pre = pre;
   tl.ln = lens;

@@ -21,8 +21,20 @@ cudaError_t launch_split_t(const CUtensorMap& tk, const CUtensorMap& tv, const S
     if (e != cudaSuccess) return e;
     configured_device.store(dev, std::memory_order_release);
   }
-  fd_split_kernel<C><<<grid, C::kThreads, C::kSmemAlloc, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the kernel may be scheduled while the
+  // kernel before it on the stream is still finishing; it touches no memory
+  // before griddepcontrol.wait, so only its set-up overlaps the earlier kernel.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fd_split_kernel<C>, tk, tv, p);
 }
 
 template <class KV>
