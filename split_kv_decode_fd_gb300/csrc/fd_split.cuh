@@ -149,7 +149,7 @@ struct SplitCfg {
   static constexpr int kLenOff = kFinOff + kPubHeads * 8;
   static constexpr int kPreOff = kLenOff + (kAutoMaxBatch + 4) * 4;
   static constexpr int kBarOff = kPreOff + (kAutoMaxBatch + 4) * 4;
-  static constexpr int kFlagOff = kBarOff + (2 * kStages + 4) * 8;
+  static constexpr int kFlagOff = kBarOff + (2 * kStages + 5) * 8;
   static constexpr int kBytes = kFlagOff + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;
   static_assert(kSmemAlloc <= 232448, "shared memory over the sm_100 limit");
@@ -215,11 +215,38 @@ struct GlobalPartials {
   }
 };
 
+// The merge's weights, computed by one warp for one head: lane holds the split
+// states k = r*32 + lane (r < kMergeKR) as (mk[r], lk[r]), with l = 0 for k at
+// or past the count.  `mx` is the largest m over splits with l > 0 (already
+// reduced over the warp); wk[r] = exp2((m_k - mx) log2 e) (0 for an empty
+// split) and lsum is this lane's part of L = sum_k w_k l_k.  Shared by every
+// merge path so that they give identical bits.
+constexpr int kMergeKR = 4;
+
+__device__ __forceinline__ float merge_max(const float (&mk)[kMergeKR], const float (&lk)[kMergeKR]) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int r = 0; r < kMergeKR; ++r)
+    if (lk[r] > 0.f) mx = fmaxf(mx, mk[r]);
+  return mx;
+}
+
+__device__ __forceinline__ float merge_weights(const float (&mk)[kMergeKR], const float (&lk)[kMergeKR], float mx,
+                                               float (&wk)[kMergeKR]) {
+  float lsum = 0.f;
+#pragma unroll
+  for (int r = 0; r < kMergeKR; ++r) {
+    wk[r] = lk[r] > 0.f ? exp2f((mk[r] - mx) * kLog2e) : 0.f;
+    lsum = fmaf(wk[r], lk[r], lsum);
+  }
+  return lsum;
+}
+
 template <int D, class P>
 __device__ __forceinline__ void merge_head(const P& src, int count, float* out_row, float* lse_slot, int lane,
                                            float* wsm) {
   constexpr int EPL = D / 32;
-  constexpr int KR = 4;                 // splits per lane whose (m, l) stay in registers: count <= 128
+  constexpr int KR = kMergeKR;          // splits per lane whose (m, l) stay in registers: count <= 128
   constexpr int NB = 128 / EPL;         // splits per batch of O loads (128 registers)
   // Round trip 1: every (m, l) and the first batch of O slices, all in flight together.
   float mk[KR], lk[KR];
@@ -240,10 +267,7 @@ __device__ __forceinline__ void merge_head(const P& src, int count, float* out_r
     for (int e = 0; e < EPL; ++e) v[j][e] = 0.f;
     if (j < count) src.slice(j, lane, v[j]);
   }
-  float mx = -INFINITY;
-#pragma unroll
-  for (int r = 0; r < KR; ++r)
-    if (lk[r] > 0.f) mx = fmaxf(mx, mk[r]);
+  float mx = merge_max(mk, lk);
   for (int k = KR * 32 + lane; k < count; k += 32)
     if (src.l(k) > 0.f) mx = fmaxf(mx, src.m(k));
   mx = warp_max(mx);
@@ -254,12 +278,7 @@ __device__ __forceinline__ void merge_head(const P& src, int count, float* out_r
     return;
   }
   float wk[KR];
-  float lsum = 0.f;
-#pragma unroll
-  for (int r = 0; r < KR; ++r) {
-    wk[r] = lk[r] > 0.f ? exp2f((mk[r] - mx) * kLog2e) : 0.f;
-    lsum = fmaf(wk[r], lk[r], lsum);
-  }
+  float lsum = merge_weights(mk, lk, mx, wk);
   for (int k = KR * 32 + lane; k < count; k += 32) {
     const float lv = src.l(k);
     if (lv > 0.f) lsum = fmaf(exp2f((src.m(k) - mx) * kLog2e), lv, lsum);
@@ -336,6 +355,9 @@ struct PieceIter {
       : walk(tl, p_.B, p_.hv, walk_active(p_, total) ? total : 0, walk_grid(p_, total),
              walk_active(p_, total) ? (int32_t)blockIdx.x : 0),
         p(p_), balanced(p_.n_splits == 0), pending(p_.n_splits != 0) {}
+
+  // Does this CTA have a piece after the one last returned?
+  __device__ __forceinline__ bool more() const { return balanced ? !walk.done() : pending; }
 
   __device__ __forceinline__ bool next(Piece& pc) {
     if (balanced) {
@@ -508,6 +530,120 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
       if (j == stalled) continue;
       if (!mbar_wait_for(full + (j % C::kStages), (j / C::kStages) & 1, wait_limit(p))) raise_error(p.err, kErrTimeout);
     }
+  }
+}
+
+// The last arriver's merge of a whole (b, virtual KV head), for a CTA with no
+// piece after this one: its K/V ring is idle, so the pair's partial outputs
+// come into it with one bulk copy (one round trip to L2 for all heads and
+// splits) while the threads load every (m, l) beside it; the weights and the
+// weighted sums then run out of shared memory.  The arithmetic per output
+// element is merge_head's (same weights, same four interleaved partial sums in
+// increasing k, same final division), so both give identical bits.
+// State (h, k) of the pair is partial index base0 + h*hs + k*stride; all
+// n_states indices lie in [base0, base0 + n_states).  count <= 128.
+template <class C>
+__device__ __forceinline__ void merge_pair_smem(const SplitParams& p, uint8_t* smem, uint64_t* mbar, size_t base0,
+                                                int n_states, int count, int nh, int hs, int stride, float* out_rows,
+                                                float* lse_slots) {
+  constexpr int D = C::D, EPL = D / 32, W = C::kWarps, kCons = W * 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* so = reinterpret_cast<float*>(smem);  // [n_states, D]
+  float* sm = so + (size_t)n_states * D;       // [n_states]
+  float* sl = sm + n_states;                   // [n_states]
+  float* sw = sl + n_states;                   // [nh, 128] weights
+  float* shead = sw + nh * 128;                // [nh, 2] (max, L)
+  const uint32_t obytes = (uint32_t)n_states * D * 4;
+  if (tid == 0) {
+    // the ring's reads by the consumers (generic proxy) come before these async-proxy writes
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(mbar, obytes);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.o_part + base0 * D);
+    constexpr uint32_t kChunk = 32768;
+    for (uint32_t off = 0; off < obytes; off += kChunk)
+      bulk_load(reinterpret_cast<uint8_t*>(so) + off, src + off, obytes - off < kChunk ? obytes - off : kChunk, mbar);
+  }
+  for (int i = tid; i < n_states; i += kCons) {
+    sm[i] = __ldcg(p.m_part + base0 + i);
+    sl[i] = __ldcg(p.l_part + base0 + i);
+  }
+  named_barrier(1, kCons);
+  for (int h = warp; h < nh; h += W) {
+    float mk[kMergeKR], lk[kMergeKR], wk[kMergeKR];
+#pragma unroll
+    for (int r = 0; r < kMergeKR; ++r) {
+      const int k = r * 32 + lane;
+      mk[r] = -INFINITY;
+      lk[r] = 0.f;
+      if (k < count) {
+        mk[r] = sm[h * hs + k * stride];
+        lk[r] = sl[h * hs + k * stride];
+      }
+    }
+    const float mx = warp_max(merge_max(mk, lk));
+    float L = 0.f;
+    if (mx != -INFINITY) {
+      L = warp_sum(merge_weights(mk, lk, mx, wk));
+    } else {
+#pragma unroll
+      for (int r = 0; r < kMergeKR; ++r) wk[r] = 0.f;
+    }
+#pragma unroll
+    for (int r = 0; r < kMergeKR; ++r) sw[h * 128 + r * 32 + lane] = wk[r];
+    if (lane == 0) {
+      shead[2 * h] = mx;
+      shead[2 * h + 1] = L;
+    }
+  }
+  if (!mbar_wait_for(mbar, 0, wait_limit(p))) {
+    raise_error(p.err, kErrTimeout);
+    mbar_wait_for(mbar, 0, wait_limit(p));  // give the copy its chance to land before the CTA leaves
+  }
+  named_barrier(1, kCons);
+  for (int item = tid; item < nh * 32; item += kCons) {
+    const int h = item >> 5, j = item & 31;
+    const float mx = shead[2 * h], L = shead[2 * h + 1];
+    float* orow = out_rows + (size_t)h * D + j * EPL;
+    if (mx == -INFINITY) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) orow[e] = 0.f;
+      if (lse_slots && j == 0) lse_slots[h] = -INFINITY;
+      continue;
+    }
+    float acc[4][EPL];
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4)
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[s4][e] = 0.f;
+    const float* wrow = sw + h * 128;
+    const float* obase = so + (size_t)h * hs * D + j * EPL;
+    for (int k0 = 0; k0 < count; k0 += 4) {
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int k = k0 + jj;
+        if (k < count) {
+          const float w = wrow[k];
+          const float* v = obase + (size_t)k * stride * D;
+          float vv[EPL];
+          if constexpr (EPL == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(v);
+            vv[0] = x.x;
+            vv[1] = x.y;
+            vv[2] = x.z;
+            vv[3] = x.w;
+          } else {
+            const float2 x = *reinterpret_cast<const float2*>(v);
+            vv[0] = x.x;
+            vv[1] = x.y;
+          }
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[jj][e] = fmaf(w, vv[e], acc[jj][e]);
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) orow[e] = (((acc[0][e] + acc[1][e]) + acc[2][e]) + acc[3][e]) / L;
+    if (lse_slots && j == 0) lse_slots[h] = mx + logf(L);
   }
 }
 
@@ -961,10 +1097,21 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
         }
         // Head h, split k: state base0 + h*hs + k*stride.
         const size_t hs = balanced ? 1 : (size_t)p.n_splits;
-        for (int h = warp; h < nh; h += W) {
-          const GlobalPartials<D> src{p.o_part, p.m_part, p.l_part, base0 + h * hs, stride};
-          merge_head<D>(src, count, p.out + ((size_t)pc.b * p.Hq + head0 + h) * D,
-                        p.lse ? p.lse + (size_t)pc.b * p.Hq + head0 + h : nullptr, lane, obuf + warp * 128);
+        // With no piece after this one, the ring is idle: merge out of shared memory.
+        const int n_states = balanced ? count * G : nh * count;
+        const bool in_smem = C::kMma && !pieces.more() && !*abort_flag && count <= kMergeKR * 32 &&
+                             (size_t)n_states * (D + 2) * 4 + (size_t)nh * 130 * 4 <=
+                                 (size_t)C::kStages * C::kStageBytes;
+        if (in_smem) {
+          merge_pair_smem<C>(p, smem, full + 2 * C::kStages + 4, base0, n_states, count, nh, (int)hs, (int)stride,
+                             p.out + ((size_t)pc.b * p.Hq + head0) * D,
+                             p.lse ? p.lse + (size_t)pc.b * p.Hq + head0 : nullptr);
+        } else {
+          for (int h = warp; h < nh; h += W) {
+            const GlobalPartials<D> src{p.o_part, p.m_part, p.l_part, base0 + h * hs, stride};
+            merge_head<D>(src, count, p.out + ((size_t)pc.b * p.Hq + head0 + h) * D,
+                          p.lse ? p.lse + (size_t)pc.b * p.Hq + head0 + h : nullptr, lane, obuf + warp * 128);
+          }
         }
         if (tid == 0) p.counters[pair] = 0;  // ready for the next call
       }
@@ -1005,6 +1152,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(bars + 2 * C::kStages + i, 1);                               // q full
       mbar_init(bars + 2 * C::kStages + 2 + i, C::kWide ? C::kWarps : 1);    // q empty
     }
+    mbar_init(bars + 2 * C::kStages + 4, 1);  // the pair merge's bulk copy (merge_pair_smem)
     *abort_flag = 0;
     fence_barrier_init();
   }
