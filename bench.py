@@ -31,6 +31,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode-attn µs/step; KV-read HBM GB/s as % of GB300 peak (1 GPU)"
+L2_BYTES = 129 * 1000 * 1000    # GB300 L2
+FLUSH_BYTES = 256 << 20         # written between launches when the inputs would stay in L2
 DEFAULT_WORKLOAD = 3
 FALLBACK_HBM_GBS = 6800.0
 
@@ -210,6 +212,25 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
 def blas_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
@@ -306,7 +327,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": spec.name, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv,
                                         "D": spec.D, "T": spec.T_cap, "kv_dtype": spec.kv_dtype},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": note},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "cpu_model": cpu_model(), "kind": "oracle",
+                         "sample": note},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -446,9 +468,39 @@ def run_fdecode(args):
     achieved = step_bytes / (mean_launch_us * 1e-6) / 1e9
     peak, peak_src = measured_peak()
 
+    # ---- inputs that fit in L2: the back-to-back figure above is warm (L2-resident).  The cold
+    # figure flushes L2 with a 256 MB write before every launch (outside the events) and times
+    # each launch with events on its stream; it becomes the line's value.
+    l2_note = f"inputs {kv_bytes / 1e6:.0f} MB > 129 MB L2; no flush"
+    warm = None
+    timed_launches = K * (2 if args.unfused else 1)
+    if kv_bytes < L2_BYTES:
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        n_cold = max(20, min(200, K))
+        cold_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_cold)]
+        for i, (a, b) in enumerate(cold_ev):
+            flush.fill_(i & 0xFF)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        cold_us = [a.elapsed_time(b) * 1e3 for a, b in cold_ev]
+        timed_launches = n_cold * (2 if args.unfused else 1)
+        del flush
+        warm = {"us_per_step": ms_per_step * 1e3, "value": value, "unit": "GB/s",
+                "method": "one CUDA graph of K back-to-back launches, inputs L2-resident"}
+        ms_per_step = statistics.mean(cold_us) * 1e-3
+        value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+        mean_launch_us = ms_per_step * 1e3
+        achieved = step_bytes / (mean_launch_us * 1e-6) / 1e9
+        l2_note = (f"inputs {kv_bytes / 1e6:.1f} MB < 129 MB L2: L2 flushed by a {FLUSH_BYTES >> 20} MB write "
+                   f"before each of {n_cold} launches, each timed with events on its stream "
+                   f"(~3 us of event overhead included); p10/p50/p90 "
+                   f"{[round(x, 2) for x in statistics.quantiles(cold_us, n=10)[0::4]]} us")
+
     # ---- end to end: host q in, host out/lse back (fd_decode_host; with rows, copies around fd_decode_rows)
     q_host = (q_rows if n_q > 1 else case.q).cpu().pin_memory()
-    lens_host = None if case.seq_lens is None else case.seq_lens.cpu()
+    lens_host = None if case.seq_lens is None else case.seq_lens.cpu().pin_memory()
     out_h = torch.empty(rows_shape + (spec.D,), dtype=torch.float32, pin_memory=True)
     lse_h = torch.empty(rows_shape, dtype=torch.float32, pin_memory=True)
     ws_h = fd.Workspace()
@@ -484,10 +536,11 @@ def run_fdecode(args):
             lse_h.copy_(lse_d, non_blocking=True)
             torch.cuda.current_stream(device).synchronize()
     else:
-        def e2e_step():
-            fd.decode_host(q_host, case.k, case.v, seq_lens_host=lens_host, max_seq_len=case.max_seq_len,
-                           block_table=case.block_table, scale=spec.scale, n_splits=spec.n_splits,
-                           out_host=out_h, lse_host=lse_h, workspace=ws_h)
+        # a decode loop's view: the same pinned host buffers every step, arguments marshalled once
+        e2e_api = "fd_decode_host via HostDecoder" if not args.unfused else e2e_api
+        e2e_step = fd.HostDecoder(q_host, case.k, case.v, seq_lens_host=lens_host, max_seq_len=case.max_seq_len,
+                                  block_table=case.block_table, scale=spec.scale, n_splits=spec.n_splits,
+                                  out_host=out_h, lse_host=lse_h, workspace=ws_h)
 
     for _ in range(max(3, args.warmup)):
         e2e_step()
@@ -511,8 +564,8 @@ def run_fdecode(args):
     cpu = None
     if world == 1 and not args.no_cpu_baseline and n_q == 1 and not args.append and not args.unfused:
         v, note, el = OracleSampler(case).whole_groups(args.cpu_seconds)
-        cpu = {"value": v, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle", "sample": note,
-               "seconds": round(el, 2)}
+        cpu = {"value": v, "unit": "GB/s", "cores": blas_threads(), "cpu_model": cpu_model(), "kind": "oracle",
+               "sample": note, "seconds": round(el, 2)}
 
     gpd = fd.workspace_status(ws)
     g = spec.Hq * n_q // spec.Hkv
@@ -528,11 +581,13 @@ def run_fdecode(args):
                    "T": spec.T_cap, "kv_dtype": spec.kv_dtype, "q_dtype": "f32", "layout": spec.layout,
                    "rows": n_q, "append": bool(args.append),
                    "kv_bytes_per_step": kv_bytes, "bytes_per_step": step_bytes,
-                   "l2": f"inputs {kv_bytes / 1e6:.0f} MB > 129 MB L2; no flush",
+                   "l2": l2_note,
                    "plan": "balanced" if spec.n_splits == 0 else f"n_splits={spec.n_splits}",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "kernel": f"fd_split_kernel<D={spec.D},{spec.kv_dtype},G={gpad}> (fused LSE merge)",
-                   "launch": "one CUDA graph of K fd_decode-family calls" if graph is not None else "K stream launches",
+                   "launch": ("single launches after an L2 flush, events around each" if warm is not None else
+                              "one CUDA graph of K fd_decode-family calls" if graph is not None else
+                              "K stream launches"),
                    "single_launch_event_us_p10_p50_p90": [round(x, 2) for x in
                                                           statistics.quantiles(launch_us, n=10)[0::4]]},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -541,7 +596,8 @@ def run_fdecode(args):
                      "mean_launch_us": mean_launch_us},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": k_e2e, "api": e2e_api},
-        "gpu_launches": K * (2 if args.unfused else 1),
+        "warm": warm,
+        "gpu_launches": timed_launches,
         "clocks": clocks,
         "cpu_baseline": cpu,
         "kernel_status": gpd,

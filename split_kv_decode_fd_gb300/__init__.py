@@ -8,6 +8,7 @@ from .fdecode import (  # noqa: F401
     FD_AUTO_MAX_BATCH,
     FD_SPLITS_AUTO,
     FdError,
+    HostDecoder,
     KvDesc,
     Workspace,
     combine,

@@ -258,6 +258,20 @@ struct HostTiles {
   FD_HD int32_t len(int32_t b) const { return ln[b]; }
 };
 
+// Device address of host memory that is pinned and mapped into the device's
+// address space (cudaHostAlloc / cudaHostRegister under unified addressing);
+// false for pageable memory.  Asked on every call: a buffer freed and another
+// allocated at the same address must not inherit the old answer.
+bool host_mapped(const void* host, float** dev) {
+  cudaPointerAttributes a;
+  void* d = nullptr;
+  if (cudaPointerGetAttributes(&a, host) == cudaSuccess && a.type == cudaMemoryTypeHost && a.devicePointer)
+    d = a.devicePointer;
+  cudaGetLastError();  // a pageable pointer may leave an error behind on older runtimes
+  *dev = static_cast<float*>(d);
+  return d != nullptr;
+}
+
 }  // namespace
 
 extern "C" {
@@ -561,15 +575,24 @@ fd_status fd_decode_host(const float* q_host, const fd_kv_desc* kv, float* out_h
   float* lse_dev = reinterpret_cast<float*>(ws + w.lse_stage);
   int32_t* len_dev = reinterpret_cast<int32_t*>(ws + w.len_stage);
   const size_t qbytes = (size_t)B * Hq * D * 4;
+  // Outputs in pinned host memory that the device can address are written by
+  // the kernels directly (no staging, no copy back); others go through the
+  // workspace and a copy.
+  float* out_k = out_host;
+  float* lse_k = lse_host;
+  if (!host_mapped(out_host, &out_k) || !aligned16(out_k)) out_k = nullptr;
+  if (lse_host && !host_mapped(lse_host, &lse_k)) lse_k = nullptr;
   if (cudaMemcpyAsync(q_dev, q_host, qbytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return FD_ERR_CUDA;
   if (seq_lens_host &&
       cudaMemcpyAsync(len_dev, seq_lens_host, (size_t)B * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return FD_ERR_CUDA;
-  st = fd_decode(q_dev, kv, out_dev, lse_host ? lse_dev : nullptr, B, Hq, Hkv, seq_lens_host ? len_dev : nullptr,
-                 max_seq_len, D, scale, n_splits, workspace, workspace_bytes, stream);
+  st = fd_decode(q_dev, kv, out_k ? out_k : out_dev, lse_host ? (lse_k ? lse_k : lse_dev) : nullptr, B, Hq, Hkv,
+                 seq_lens_host ? len_dev : nullptr, max_seq_len, D, scale, n_splits, workspace, workspace_bytes,
+                 stream);
   if (st != FD_OK) return st;
-  if (cudaMemcpyAsync(out_host, out_dev, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return FD_ERR_CUDA;
-  if (lse_host &&
+  if (!out_k && cudaMemcpyAsync(out_host, out_dev, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FD_ERR_CUDA;
+  if (lse_host && !lse_k &&
       cudaMemcpyAsync(lse_host, lse_dev, (size_t)B * Hq * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return FD_ERR_CUDA;
   return cudaStreamSynchronize(s) == cudaSuccess ? FD_OK : FD_ERR_CUDA;

@@ -17,7 +17,7 @@ import numpy as np
 
 __all__ = [
     "FdError", "KvDesc", "library_path", "load_library", "workspace_bytes", "split_size", "plan_pieces",
-    "Workspace", "decode", "decode_rows", "append_decode", "prefill", "attend", "attend_backend", "decode_host", "decode_static", "static_status", "split_partial", "combine", "workspace_status",
+    "Workspace", "decode", "decode_rows", "append_decode", "prefill", "attend", "attend_backend", "decode_host", "HostDecoder", "decode_static", "static_status", "split_partial", "combine", "workspace_status",
 ]
 
 FD_OK, FD_ERR_INVALID_ARG, FD_ERR_UNSUPPORTED, FD_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3
@@ -459,6 +459,54 @@ def decode_host(q_host, k, v, *, seq_lens_host=None, max_seq_len=None, block_tab
                                _stream_handle(k.device, stream))
     _check(st, "fd_decode_host")
     return out_host, lse_host
+
+
+class HostDecoder:
+    """``fd_decode_host`` with its arguments marshalled once, for a decode loop
+    that passes the same host buffers and KV cache every step.
+
+    ``q_host`` ``[B, Hq, D]`` fp32, ``out_host`` ``[B, Hq, D]`` and ``lse_host``
+    ``[B, Hq]`` (optional), ``seq_lens_host`` ``[B]`` int32 (optional) are CPU
+    tensors whose contents the caller rewrites between steps; pinned buffers
+    (``pin_memory=True``) let the copies run asynchronously, and pinned outputs
+    are written by the kernels directly.  Calling the object runs one
+    synchronous step and returns ``(out_host, lse_host)``.
+    """
+
+    def __init__(self, q_host, k, v, *, out_host=None, lse_host=None, seq_lens_host=None, max_seq_len=None,
+                 block_table=None, scale=None, n_splits=FD_SPLITS_AUTO, workspace: Optional[Workspace] = None,
+                 stream=None):
+        torch = _torch()
+        if q_host.is_cuda or q_host.dtype != torch.float32 or not q_host.is_contiguous():
+            raise ValueError("q_host must be a contiguous fp32 CPU tensor")
+        self._kv = _kv_desc(k, v, block_table)
+        B, Hq, Hkv, D, max_seq_len = _geometry(q_host, k, block_table, seq_lens_host, max_seq_len)
+        if scale is None:
+            scale = 1.0 / math.sqrt(D)
+        if out_host is None:
+            out_host = torch.empty((B, Hq, D), dtype=torch.float32, pin_memory=True)
+        for t, name, shape, dt in ((out_host, "out_host", (B, Hq, D), torch.float32),
+                                   (lse_host, "lse_host", (B, Hq), torch.float32),
+                                   (seq_lens_host, "seq_lens_host", (B,), torch.int32)):
+            if t is not None and (t.is_cuda or t.dtype != dt or not t.is_contiguous() or tuple(t.shape) != shape):
+                raise ValueError(f"{name} must be a contiguous {dt} CPU tensor of shape {shape}")
+        ws = workspace or _default_workspace(k.device)
+        buf = ws.get(workspace_bytes(B, Hq, Hkv, D, n_splits), k.device)
+        self.q_host, self.out_host, self.lse_host, self.seq_lens_host = q_host, out_host, lse_host, seq_lens_host
+        self._keep = (k, v, block_table, buf)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int32
+        self._fn = _lib().fd_decode_host
+        self._args = (vp(q_host.data_ptr()), ctypes.byref(self._kv), vp(out_host.data_ptr()),
+                      vp(lse_host.data_ptr() if lse_host is not None else None), i32(B), i32(Hq), i32(Hkv),
+                      vp(seq_lens_host.data_ptr() if seq_lens_host is not None else None), i32(max_seq_len), i32(D),
+                      ctypes.c_float(scale), i32(int(n_splits)), vp(buf.data_ptr()), ctypes.c_size_t(buf.numel()),
+                      vp(_stream_handle(k.device, stream)))
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != FD_OK:
+            raise FdError(st, "fd_decode_host")
+        return self.out_host, self.lse_host
 
 
 def split_partial(q, k, v, n_splits: int, *, seq_lens=None, max_seq_len=None, block_table=None, scale=None,

@@ -245,6 +245,28 @@ def test_decode_host_matches_device():
     assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_decoder_matches_device(pinned):
+    """HostDecoder (fd_decode_host, arguments marshalled once) over several steps: pinned
+    outputs are written by the kernels directly, pageable ones come back by copy."""
+    case = make_case(CONFIGS[4], "cuda")
+    out_d, lse_d = run(case)
+    q_host = case.q.cpu().pin_memory()
+    lens_host = case.seq_lens.cpu().pin_memory()
+    out_h = torch.full((case.spec.B, case.spec.Hq, case.spec.D), float("nan"), pin_memory=pinned)
+    lse_h = torch.full((case.spec.B, case.spec.Hq), float("nan"), pin_memory=pinned)
+    dec = fd.HostDecoder(q_host, case.k, case.v, seq_lens_host=lens_host, max_seq_len=case.max_seq_len,
+                         scale=case.spec.scale, out_host=out_h, lse_host=lse_h)
+    for step in range(3):
+        out_h.fill_(float("nan"))
+        o, l = dec()
+        assert o is out_h and l is lse_h
+        assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu()), f"step {step}"
+    ref_out, ref_lse = oracle_for(case)
+    assert_close(np64(out_h), ref_out, "out")
+    assert_close(np64(lse_h), ref_lse, "lse")
+
+
 def test_bad_block_table_entry_is_reported_not_faulted():
     spec = small_spec("badpage", 2, 4, 2, 128, 256, layout="paged", lengths="uniform:100:256", seed=9)
     case = make_case(spec, "cuda")
