@@ -346,8 +346,8 @@ FD_API int64_t fd_plan_pieces(int32_t B, int32_t Hq, int32_t Hkv, int32_t kv_dty
  * default), records FD_ERR_TIMEOUT in the error word, lets the copies it
  * issued land and exits, so the context stays usable.  With stage >= 0, the
  * split kernels launched afterwards (fd_decode and every call built on it,
- * fd_split_partial) skip the copies of stage number `stage` in their first
- * CTA, so the wait for that stage runs out; wait_limit_ns > 0 shortens every
+ * fd_split_partial) skip the copies of stage number `stage` in every CTA that
+ * reaches it, so the waits for that stage run out; wait_limit_ns > 0 shortens every
  * wait of those kernels to that many nanoseconds (0 keeps the default).  The
  * call's output is then undefined and fd_workspace_status (or
  * fd_static_status) reports FD_ERR_TIMEOUT; the workspace stays valid for the

@@ -249,12 +249,14 @@ fd_status launch(const fd_kv_desc* kv, int D, const SplitParams& p, dim3 grid, c
   return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
-// Host copy of the per-sequence tile table, for the plan inspector.
+// Host copy of the per-sequence cost-unit table, for the plan inspector.
 struct HostTiles {
-  const int32_t* pre;
+  const int64_t* pre;
   const int32_t* ln;
-  FD_HD int32_t prefix(int32_t b) const { return pre[b]; }
-  FD_HD int32_t tiles(int32_t b) const { return pre[b + 1] - pre[b]; }
+  int32_t piece_units;
+  FD_HD int32_t piece() const { return piece_units; }
+  FD_HD int64_t prefix(int32_t b) const { return pre[b]; }
+  FD_HD int32_t tiles(int32_t b) const { return ceil_div(ln[b], kPlanTile); }
   FD_HD int32_t len(int32_t b) const { return ln[b]; }
 };
 
@@ -603,9 +605,12 @@ int64_t fd_plan_pieces(int32_t B, int32_t Hq, int32_t Hkv, int32_t kv_dtype, con
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_seq_len < 0 || n_splits < 0) return -1;
   if (kv_dtype != FD_F32 && kv_dtype != FD_BF16) return -1;
   const Groups gr = make_groups(Hq, Hkv, group_cap(kv_dtype));
-  std::vector<int32_t> ln(B), pre(B + 1, 0);
+  std::vector<int32_t> ln(B);
+  std::vector<int64_t> pre(B + 1, 0);
   for (int b = 0; b < B; ++b) ln[b] = clamp_len(seq_lens_host ? seq_lens_host[b] : max_seq_len, max_seq_len);
-  for (int b = 0; b < B; ++b) pre[b + 1] = pre[b] + ceil_div(ln[b], kPlanTile);
+  // the kernels charge a piece per pair only when given per-sequence lengths
+  const int32_t piece = seq_lens_host ? kPieceUnits : 0;
+  for (int b = 0; b < B; ++b) pre[b + 1] = pre[b] + pair_units(ceil_div(ln[b], kPlanTile), piece);
   int64_t count = 0;
   auto emit = [&](int32_t cta, const Piece& pc, int32_t npieces) {
     if (pieces && count < capacity) {
@@ -622,14 +627,14 @@ int64_t fd_plan_pieces(int32_t B, int32_t Hq, int32_t Hkv, int32_t kv_dtype, con
   };
   if (n_splits == 0) {
     if (grid < 1) return -1;
-    HostTiles tl{pre.data(), ln.data()};
+    HostTiles tl{pre.data(), ln.data(), piece};
     const int64_t total = (int64_t)gr.hv * pre[B];
     if (total == 0) return 0;
     const int32_t used = balanced_ctas(total, grid);
     for (int32_t cta = 0; cta < used; ++cta) {
       BalancedWalk<HostTiles> w(tl, B, gr.hv, total, used, cta);
-      while (!w.done()) {
-        const Piece pc = w.next();
+      Piece pc;
+      while (w.next(pc)) {
         int32_t first, last;
         balanced_pair_ctas(tl, gr.hv, total, used, pc.b, pc.vkv, &first, &last);
         emit(cta, pc, last - first + 1);

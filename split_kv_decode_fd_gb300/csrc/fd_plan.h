@@ -8,22 +8,31 @@
 //
 //  * explicit: exactly that grid.  Split s of (b, kv head) covers tokens
 //    [s*S, min((s+1)*S, L_b)), S = 16 * ceil(ceil(max_len / n_splits) / 16).
-//  * balanced ("auto"): every (b, virtual kv head) sequence is cut into tiles
-//    of kPlanTile tokens; the tiles of all sequences are laid end to end in
-//    (b, virtual kv head, tile) order, T tiles in total, and CTA i of G takes
-//    the contiguous range [floor(i*T/G), floor((i+1)*T/G)).  A CTA range that
-//    crosses sequence boundaries yields one piece per sequence it touches.
-//    Every CTA therefore streams the same number of bytes (to one tile),
-//    whatever the mix of lengths.
+//  * balanced ("auto"): every (b, virtual kv head) sequence -- a "pair" -- is
+//    cut into tiles of kPlanTile tokens, and the pairs are laid end to end in
+//    (b, virtual kv head) order on a line of cost units: a pair costs
+//    kPieceUnits (the work a CTA spends on one more piece: its merge and the
+//    pipeline bubble around it, about a tile and a quarter of streaming,
+//    measured) followed by kTileUnits per tile.  When all sequences have the
+//    same length the pairs line up with the CTA ranges on their own and the
+//    per-pair charge is left out (piece units 0).  CTA i of G takes the units
+//    [floor(i*U/G), floor((i+1)*U/G)) of the U in all, and with them every tile
+//    whose unit position falls inside; a range that crosses pair boundaries
+//    yields one piece per pair it touches.  Every CTA therefore gets the same
+//    cost (to a tile), so a CTA that meets many short sequences streams fewer
+//    keys.  A tile t of a pair starting at unit v sits at unit
+//    v + kPieceUnits + kTileUnits*t.
 //
 // A "virtual kv head" is one KV head together with a sub-group of at most
 // max_group of the query heads that share it (16 for bf16 caches, whose
 // tensor-core engine takes sixteen heads; 8 for fp32); when g <= max_group
 // there is one sub-group per KV head.
 //
-// The balanced plan uses G = min(CTAs launched, T) CTAs, so that every range
-// holds at least one tile and the CTAs holding one sequence are consecutive;
-// extra CTAs idle.
+// The balanced plan uses G = min(CTAs launched, U / kTileUnits) CTAs: every
+// range is at least a tile's worth of units wide, so a range that lies inside
+// a pair's tiles holds at least one of them and the CTAs holding one pair are
+// consecutive (a CTA whose range falls between two pairs' tiles may hold none
+// and idles).
 //
 // Output slots of the balanced plan: the piece of pair p (= b*HV + vkv) run by
 // CTA i goes to slot p + i.  For fixed i the pairs touched are consecutive,
@@ -90,11 +99,6 @@ FD_HD void vkv_heads(const Groups& gr, int32_t vkv, int32_t* head0, int32_t* nhe
 
 FD_HD int32_t kv_head_of_vkv(const Groups& gr, int32_t vkv) { return vkv / gr.nsub; }
 
-// CTAs that take part in the balanced plan of `total` tiles on `launched` CTAs.
-FD_HD int32_t balanced_ctas(int64_t total, int32_t launched) {
-  return total < (int64_t)launched ? (int32_t)total : launched;
-}
-
 // Exact floor(n / d) for 0 <= n, 0 < d; 32-bit division whenever both fit
 // (a 64-bit division is a long instruction sequence on the GPU, and the plan
 // is walked at the start of every CTA and of every piece).
@@ -103,13 +107,38 @@ FD_HD int64_t div_floor(int64_t n, int64_t d) {
   return n / d;
 }
 
-// Balanced plan: CTA range bounds and the CTA owning a flat tile.
-FD_HD int64_t range_begin(int64_t total, int32_t grid, int32_t cta) {
-  return div_floor(total * (int64_t)cta, (int64_t)grid);
+// Cost units of the balanced plan (see the top of this file).
+constexpr int kTileUnits = 4;
+constexpr int kPieceUnits = 5;
+
+// Units of one pair with `tiles` tiles (none for an empty sequence); `piece`
+// is the plan's charge per pair (kPieceUnits, or 0 when every sequence has the
+// same length: the pairs then line up with the CTA ranges as well as the
+// plain split allows, and the charge would only shift work around).
+FD_HD int64_t pair_units(int32_t tiles, int32_t piece) {
+  return tiles > 0 ? (int64_t)kTileUnits * tiles + piece : 0;
 }
 
-FD_HD int32_t cta_of_tile(int64_t total, int32_t grid, int64_t tile) {
-  return (int32_t)div_floor((tile + 1) * (int64_t)grid - 1, total);
+// CTAs that take part in the balanced plan of `units` cost units on `launched` CTAs.
+FD_HD int32_t balanced_ctas(int64_t units, int32_t launched) {
+  const int64_t cap = units / kTileUnits;
+  return cap < (int64_t)launched ? (int32_t)cap : launched;
+}
+
+// Balanced plan: CTA range bounds (in units) and the CTA owning a unit.
+FD_HD int64_t range_begin(int64_t units, int32_t grid, int32_t cta) {
+  return div_floor(units * (int64_t)cta, (int64_t)grid);
+}
+
+FD_HD int32_t cta_of_unit(int64_t units, int32_t grid, int64_t u) {
+  return (int32_t)div_floor((u + 1) * (int64_t)grid - 1, units);
+}
+
+// Index of the first tile of the pair starting at unit v whose unit position
+// is at or after unit r (may be past the pair's last tile).
+FD_HD int32_t first_tile_at(int64_t r, int64_t v, int32_t piece) {
+  const int64_t d = r - v - piece;
+  return d <= 0 ? 0 : (int32_t)div_floor(d + kTileUnits - 1, kTileUnits);
 }
 
 // One unit of work: a run of consecutive keys of one (b, virtual kv head).
@@ -120,76 +149,90 @@ struct Piece {
   int32_t len;                 // L_b, the valid length of sequence b
 };
 
-// Walk of one CTA over its tile range in the balanced plan.  `Tiles` maps a
-// sequence index b to (tile_prefix(b), tiles(b), len(b)), with tile_prefix the
-// number of tiles of sequences < b per virtual kv head.
+// Walk of one CTA over its unit range in the balanced plan.  `Tiles` maps a
+// sequence index b to prefix(b) (the units of the pairs of sequences < b, per
+// virtual kv head), tiles(b) and len(b), and gives the plan's charge per pair
+// as piece().
 template <class Tiles>
 struct BalancedWalk {
   const Tiles& tl;
   int32_t B, hv, cta;
-  int64_t flat, end;     // current flat tile, end of range
-  int32_t b, vkv, tile;  // position of `flat`
+  int64_t pos, end;  // current unit, end of range
+  int32_t b, vkv;    // the pair holding `pos`
+  int64_t v;         // its first unit
 
-  FD_HD BalancedWalk(const Tiles& t, int32_t B_, int32_t hv_, int64_t total, int32_t grid,
-                     int32_t cta_)
+  FD_HD BalancedWalk(const Tiles& t, int32_t B_, int32_t hv_, int64_t units, int32_t grid, int32_t cta_)
       : tl(t), B(B_), hv(hv_), cta(cta_) {
-    flat = range_begin(total, grid, cta);
-    end = range_begin(total, grid, cta + 1);
-    b = vkv = tile = 0;
-    if (flat < end) locate();
+    pos = range_begin(units, grid, cta);
+    end = range_begin(units, grid, cta + 1);
+    b = vkv = 0;
+    v = 0;
+    if (pos < end) locate();
   }
 
-  // Binary search for the sequence holding `flat`, then the head and tile.
+  FD_HD int64_t units_of(int32_t bb) const { return pair_units(tl.tiles(bb), tl.piece()); }
+
+  // Binary search for the sequence holding `pos`, then the pair.
   FD_HD void locate() {
     int32_t lo = 0, hi = B - 1;
-    while (lo < hi) {  // largest b with hv*prefix(b) <= flat and tiles(b) > 0
+    while (lo < hi) {  // largest b with hv*prefix(b) <= pos
       int32_t mid = (lo + hi + 1) / 2;
-      if ((int64_t)hv * tl.prefix(mid) <= flat) lo = mid; else hi = mid - 1;
+      if ((int64_t)hv * tl.prefix(mid) <= pos) lo = mid; else hi = mid - 1;
     }
     b = lo;
-    while (tl.tiles(b) == 0) ++b;  // empty sequences own no tiles
-    int64_t off = flat - (int64_t)hv * tl.prefix(b);
-    vkv = (int32_t)div_floor(off, tl.tiles(b));
-    tile = (int32_t)(off - (int64_t)vkv * tl.tiles(b));
+    while (b < B - 1 && units_of(b) == 0) ++b;  // empty sequences own no units
+    const int64_t base = (int64_t)hv * tl.prefix(b);
+    const int64_t u = units_of(b);
+    vkv = u > 0 ? (int32_t)div_floor(pos - base, u) : 0;
+    v = base + (int64_t)vkv * u;
   }
 
-  FD_HD bool done() const { return flat >= end; }
+  // Does the range hold units not walked yet?  (It may hold no further tile.)
+  FD_HD bool done() const { return pos >= end; }
 
-  // Current piece; then step past it.
-  FD_HD Piece next() {
-    Piece pc;
-    int32_t nt = tl.tiles(b);
-    int64_t left = end - flat;
-    int32_t take = (int64_t)(nt - tile) < left ? nt - tile : (int32_t)left;
-    pc.b = b;
-    pc.vkv = vkv;
-    pc.tok_begin = tile * kPlanTile;
-    int32_t e = (tile + take) * kPlanTile;
-    int32_t L = tl.len(b);
-    pc.tok_end = e < L ? e : L;
-    pc.len = L;
-    pc.slot = (b * hv + vkv) + cta;
-    flat += take;
-    tile += take;
-    if (tile == nt) {
-      tile = 0;
-      if (++vkv == hv) {
-        vkv = 0;
-        ++b;
-        while (flat < end && tl.tiles(b) == 0) ++b;
+  // The next piece of the range; false when no tile is left in it.
+  FD_HD bool next(Piece& pc) {
+    while (pos < end) {
+      const int32_t nt = tl.tiles(b);
+      const int64_t pend = v + pair_units(nt, tl.piece());
+      const int64_t stop = end < pend ? end : pend;
+      const int32_t lo = first_tile_at(pos, v, tl.piece());
+      int32_t hi = first_tile_at(stop, v, tl.piece());
+      hi = hi < nt ? hi : nt;
+      const int32_t cb = b, cv = vkv;
+      pos = stop;
+      if (pos == pend) {  // step to the next pair
+        v = pend;
+        if (++vkv == hv) {
+          vkv = 0;
+          ++b;
+          while (b < B - 1 && tl.tiles(b) == 0) ++b;
+        }
+      }
+      if (hi > lo) {
+        const int32_t L = tl.len(cb);
+        pc.b = cb;
+        pc.vkv = cv;
+        pc.tok_begin = lo * kPlanTile;
+        const int32_t e = hi * kPlanTile;
+        pc.tok_end = e < L ? e : L;
+        pc.len = L;
+        pc.slot = (cb * hv + cv) + cta;
+        return true;
       }
     }
-    return pc;
+    return false;
   }
 };
 
 // Pieces of pair p = b*hv + vkv in the balanced plan: CTAs [first, last].
 template <class Tiles>
-FD_HD void balanced_pair_ctas(const Tiles& tl, int32_t hv, int64_t total, int32_t grid, int32_t b,
-                              int32_t vkv, int32_t* first, int32_t* last) {
-  int64_t f = (int64_t)hv * tl.prefix(b) + (int64_t)vkv * tl.tiles(b);
-  *first = cta_of_tile(total, grid, f);
-  *last = cta_of_tile(total, grid, f + tl.tiles(b) - 1);
+FD_HD void balanced_pair_ctas(const Tiles& tl, int32_t hv, int64_t units, int32_t grid, int32_t b, int32_t vkv,
+                              int32_t* first, int32_t* last) {
+  const int32_t nt = tl.tiles(b);
+  const int64_t v = (int64_t)hv * tl.prefix(b) + (int64_t)vkv * pair_units(nt, tl.piece());
+  *first = cta_of_unit(units, grid, v + tl.piece());
+  *last = cta_of_unit(units, grid, v + tl.piece() + (int64_t)kTileUnits * (nt - 1));
 }
 
 }  // namespace fdk

@@ -76,8 +76,8 @@ struct SplitParams {
   void* v_cache;
   int64_t capacity;        // contiguous: rows per (b, KV head)
   // Bounded waits: every mbarrier wait gives up after wait_ns (0 = kWaitLimitNs).
-  // Testing hook: stall_it >= 0 makes the producer of CTA 0 skip the copies of
-  // its stage number stall_it, so that the consumers' wait on it runs out.
+  // Testing hook: stall_it >= 0 makes the producer of every CTA skip the copies
+  // of its stage number stall_it, so that the consumers' wait on it runs out.
   uint64_t wait_ns;
   int32_t stall_it;
 };
@@ -150,7 +150,8 @@ struct SplitCfg {
   static constexpr int kPreOff = kLenOff + (kAutoMaxBatch + 4) * 4;
   static constexpr int kBarOff = kPreOff + (kAutoMaxBatch + 4) * 4;
   static constexpr int kFlagOff = kBarOff + (2 * kStages + 5) * 8;
-  static constexpr int kBytes = kFlagOff + 16;
+  static constexpr int kDescOff = (kFlagOff + 16 + 15) / 16 * 16;  // PieceDesc per q slot
+  static constexpr int kBytes = kDescOff + 2 * 48;
   static constexpr int kSmemAlloc = kBytes + 1024;
   static_assert(kSmemAlloc <= 232448, "shared memory over the sm_100 limit");
 };
@@ -169,12 +170,13 @@ __device__ __forceinline__ void raise_error(unsigned* err, unsigned bits) {
 
 // Lengths and per-sequence tile counts seen by every thread of a CTA.
 struct CtaTiles {
-  const int32_t* pre;  // shared: tile prefix per sequence (balanced with lengths)
+  const int32_t* pre;  // shared: cost-unit prefix per sequence, per pair (balanced with lengths)
   const int32_t* ln;   // shared: clamped lengths
   int32_t ut, ul;      // uniform tile count / length when no lengths are given
   int uniform;
-  FD_HD int32_t prefix(int32_t b) const { return uniform ? b * ut : pre[b]; }
-  FD_HD int32_t tiles(int32_t b) const { return uniform ? ut : pre[b + 1] - pre[b]; }
+  FD_HD int32_t piece() const { return uniform ? 0 : kPieceUnits; }
+  FD_HD int64_t prefix(int32_t b) const { return uniform ? (int64_t)b * pair_units(ut, 0) : pre[b]; }
+  FD_HD int32_t tiles(int32_t b) const { return uniform ? ut : ceil_div(ln[b], kPlanTile); }
   FD_HD int32_t len(int32_t b) const { return uniform ? ul : ln[b]; }
 };
 
@@ -337,7 +339,21 @@ __device__ __forceinline__ void merge_head(const P& src, int count, float* out_r
   if (lse_slot && lane == 0) *lse_slot = mx + logf(L);
 }
 
-// The pieces of this CTA, in the same order for every role.
+// A piece as the producer announces it to the consumers: written to the
+// shared-memory slot of the piece's q rows before the arrival on that slot's
+// "q full" barrier, read by the consumers after their wait on it.  b < 0 ends
+// the CTA's work.
+struct PieceDesc {
+  int32_t b, vkv, tok_begin, tok_end, slot, len;
+  int32_t npieces;  // pieces of the sequence (b, vkv) over all CTAs: the arrival count
+  int32_t first;    // balanced plan: first CTA holding the sequence
+  int32_t more;     // this CTA has a piece after this one
+  int32_t has_q;    // the piece's q rows were loaded (not after an abort)
+  int32_t pad[2];
+};
+static_assert(sizeof(PieceDesc) == 48, "PieceDesc layout");
+
+// The pieces of this CTA, walked by the producer, which announces each one.
 struct PieceIter {
   BalancedWalk<CtaTiles> walk;
   const SplitParams& p;
@@ -360,11 +376,7 @@ struct PieceIter {
   __device__ __forceinline__ bool more() const { return balanced ? !walk.done() : pending; }
 
   __device__ __forceinline__ bool next(Piece& pc) {
-    if (balanced) {
-      if (walk.done()) return false;
-      pc = walk.next();
-      return true;
-    }
+    if (balanced) return walk.next(pc);
     if (!pending) return false;
     pending = false;
     const int32_t pair = blockIdx.x, s = blockIdx.y;
@@ -409,12 +421,13 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
   const int32_t step_q = p.paged ? C::kBT / p.page_size : 0;
   const int32_t step_r = p.paged ? C::kBT % p.page_size : 0;
 
+  PieceDesc* desc = reinterpret_cast<PieceDesc*>(smem + C::kDescOff);
+  const int32_t grid_used = p.n_splits == 0 ? balanced_ctas(total, (int32_t)gridDim.x) : 0;
   PieceIter pieces(p, tl, total);
   Piece pc;
-  bool waited = false;
+  bool waited = false, live = true;  // live: the consumers still take announcements
   while (pieces.next(pc)) {
-    if (!ok) break;
-    if (pc.tok_end <= pc.tok_begin) continue;
+    const bool nonempty = pc.tok_end > pc.tok_begin;
     if (!waited) {  // first memory access of this warp: q, the block table, K/V
       pdl_wait();
       waited = true;
@@ -422,18 +435,50 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
     int32_t head0, nh;
     vkv_heads(gr, pc.vkv, &head0, &nh);
     const int32_t kvh = kv_head_of_vkv(gr, pc.vkv);
+    // The piece's arrival count (the consumers' registers are scarcer than the producer's).
+    int32_t npieces = p.n_splits, first = 0;
+    if (p.n_splits == 0) {
+      int32_t last;
+      balanced_pair_ctas(tl, p.hv, total, grid_used, pc.b, pc.vkv, &first, &last);
+      npieces = last - first + 1;
+    }
+    // Announce it with its q rows.  After an abort (!ok) the pieces are still
+    // announced, without q and without tiles, so that every arrival count
+    // completes and the counters end at zero.
     if (lane == 0) {
       const uint32_t slot = qi % C::kQBufs;
-      if (!mbar_wait_for(qempty + slot, ((qi / C::kQBufs) & 1) ^ 1, wait_limit(p))) ok = false;
-      if (ok) {
-        const uint32_t bytes = (uint32_t)nh * C::D * 4;
-        mbar_arrive_expect_tx(qfull + slot, bytes);
-        bulk_load(smem + C::kQOff + slot * C::kQBytes, p.q + ((size_t)pc.b * p.Hq + head0) * C::D, bytes,
-                  qfull + slot);
+      if (!mbar_wait_for(qempty + slot, ((qi / C::kQBufs) & 1) ^ 1, wait_limit(p))) {
+        live = false;  // the consumers stopped taking pieces
+      } else {
+        const bool load_q = ok && nonempty;
+        PieceDesc* d = desc + slot;
+        d->b = pc.b;
+        d->vkv = pc.vkv;
+        d->tok_begin = pc.tok_begin;
+        d->tok_end = pc.tok_end;
+        d->slot = pc.slot;
+        d->len = pc.len;
+        d->npieces = npieces;
+        d->first = first;
+        d->more = pieces.more() ? 1 : 0;
+        d->has_q = load_q ? 1 : 0;
+        if (load_q) {
+          const uint32_t bytes = (uint32_t)nh * C::D * 4;
+          mbar_arrive_expect_tx(qfull + slot, bytes);
+          bulk_load(smem + C::kQOff + slot * C::kQBytes, p.q + ((size_t)pc.b * p.Hq + head0) * C::D, bytes,
+                    qfull + slot);
+        } else {
+          mbar_arrive(qfull + slot);
+        }
       }
     }
     ++qi;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
+    live = __shfl_sync(0xffffffffu, live, 0);
+    if (!live) {
+      ok = false;
+      break;
+    }
+    if (!ok || !nonempty) continue;
     // Paged: lane j looks up the page of row block j of a tile kPageAhead tiles
     // ahead, so the table loads -- which miss L2 once the K/V stream has
     // evicted the table -- overlap several stages.  The tile loop is unrolled
@@ -485,7 +530,7 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
         const unsigned issue = __ballot_sync(0xffffffffu, mine);
         const uint32_t stage = it % C::kStages;
         const uint32_t phase = (it / C::kStages) & 1;
-        const bool stall = p.stall_it >= 0 && it == (uint32_t)p.stall_it && blockIdx.x == 0 && blockIdx.y == 0;
+        const bool stall = p.stall_it >= 0 && it == (uint32_t)p.stall_it;
         if (lane == 0) {
           if (*abort_flag || !mbar_wait_for(empty + stage, phase ^ 1, wait_limit(p))) {
             ok = false;
@@ -519,6 +564,17 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
       }
     }
   }
+  // No more pieces: tell the consumers.
+  if (live && lane == 0) {
+    const uint32_t slot = qi % C::kQBufs;
+    if (mbar_wait_for(qempty + slot, ((qi / C::kQBufs) & 1) ^ 1, wait_limit(p))) {
+      desc[slot].b = -1;
+      mbar_arrive(qfull + slot);
+    } else {
+      ok = false;
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
   if (!ok) {
     raise_error(p.err, kErrTimeout);
     *abort_flag = 1;
@@ -948,29 +1004,35 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
   uint32_t it = 0, qi = 0;
   bool ok = true;
 
-  PieceIter pieces(p, tl, total);
-  Piece pc;
-  while (pieces.next(pc)) {
+  // The producer announces every piece of this CTA (PieceDesc, with its q rows)
+  // and then an end mark.
+  const PieceDesc* desc = reinterpret_cast<const PieceDesc*>(smem + C::kDescOff);
+  for (;;) {
+    const uint32_t qslot = qi % C::kQBufs;
+    if (!mbar_wait_for(qfull + qslot, (qi / C::kQBufs) & 1, wait_limit(p))) {
+      ok = false;
+      *abort_flag = 1;
+      break;
+    }
+    const PieceDesc& d = desc[qslot];
+    Piece pc;
+    pc.b = d.b;
+    if (pc.b < 0) break;
+    pc.vkv = d.vkv;
+    pc.tok_begin = d.tok_begin;
+    pc.tok_end = d.tok_end;
+    pc.slot = d.slot;
+    pc.len = d.len;
+    const int npieces = d.npieces;
+    const int32_t first = d.first;  // balanced: first CTA holding this sequence
+    const bool more = d.more != 0, has_q = d.has_q != 0;
     int32_t head0, nh;
     vkv_heads(gr, pc.vkv, &head0, &nh);
     const bool nonempty = pc.tok_end > pc.tok_begin;
-    // Does this piece hold the whole sequence?  Then it is the output.  (Worked
-    // out here, while the piece's first tile is still on its way, rather than
-    // after its last tile, where it would delay the merge.)
-    int npieces = 1;
-    int32_t first = 0;  // balanced: first CTA holding this sequence
     const int32_t pair = pc.b * p.hv + pc.vkv;
-    if (balanced) {
-      int32_t last;
-      balanced_pair_ctas(tl, p.hv, total, balanced_ctas(total, (int32_t)gridDim.x), pc.b, pc.vkv, &first,
-                         &last);
-      npieces = last - first + 1;
-    } else {
-      npieces = p.n_splits;
-    }
+    // Does this piece hold the whole sequence?  Then it is the output.
     const bool final_here = fused && npieces == 1;
     eng.reset();
-    const uint32_t qslot = qi % C::kQBufs;
     // Fused append: the warp owning the new token's row prefetches it now.
     const bool app = p.append && nonempty && pc.tok_end == pc.len;
     const int32_t app_t0 = pc.tok_begin + (pc.tok_end - 1 - pc.tok_begin) / C::kBT * C::kBT;  // last tile
@@ -978,19 +1040,18 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
     AppendRow<C> arow;
     if (app && warp == (app_r >> 5))
       arow.prefetch(p, pc.b, kv_head_of_vkv(gr, pc.vkv), pc.len - 1, lane, pc.vkv % gr.nsub == 0);
-    if (nonempty && ok) {
-      if (!mbar_wait_for(qfull + qslot, (qi / C::kQBufs) & 1, wait_limit(p))) {
-        ok = false;
-        *abort_flag = 1;
-      }
-      const uint32_t qaddr = sbase + C::kQOff + qslot * C::kQBytes;
+    const bool run_tiles = nonempty && ok && has_q;
+    const uint32_t qaddr = sbase + C::kQOff + qslot * C::kQBytes;
+    if (run_tiles) {
       const RowLimits rl{head0, nh, pc.len, p.n_q, p.causal};
-      if (ok) eng.begin(qaddr, p.qk_scale, rl);
-      if constexpr (C::kWide) {
-        // q is in registers now: hand the buffer back (one arrival per warp)
-        __syncwarp();
-        if (lane == 0) mbar_arrive(qempty + qslot);
-      }
+      eng.begin(qaddr, p.qk_scale, rl);
+    }
+    if constexpr (C::kWide) {
+      // q (if any) is in registers now and the piece is read: hand the slot back (one arrival per warp)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qempty + qslot);
+    }
+    if (run_tiles) {
       for (int32_t t0 = pc.tok_begin; ok && t0 < pc.tok_end; t0 += C::kBT, ++it) {
         const uint32_t stage = it % C::kStages;
         if (*abort_flag || !mbar_wait_for(full + stage, (it / C::kStages) & 1, wait_limit(p))) {
@@ -1014,9 +1075,9 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
     // ---- merge the W warp states of this piece
     named_barrier(1, kCons);  // every warp is past its last tile: the p buffers may be reused
     if constexpr (!C::kWide) {
-      if (nonempty && tid == 0) mbar_arrive(qempty + qslot);
+      if (tid == 0) mbar_arrive(qempty + qslot);  // the piece's q slot and descriptor are free
     }
-    if (nonempty) ++qi;
+    ++qi;
 
     // kPubHeads heads per round; rounds > 1 only with sixteen heads per CTA
     constexpr int PH = C::kPubHeads;
@@ -1099,7 +1160,7 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
         const size_t hs = balanced ? 1 : (size_t)p.n_splits;
         // With no piece after this one, the ring is idle: merge out of shared memory.
         const int n_states = balanced ? count * G : nh * count;
-        const bool in_smem = C::kMma && !pieces.more() && !*abort_flag && count <= kMergeKR * 32 &&
+        const bool in_smem = C::kMma && !more && !*abort_flag && count <= kMergeKR * 32 &&
                              (size_t)n_states * (D + 2) * 4 + (size_t)nh * 130 * 4 <=
                                  (size_t)C::kStages * C::kStageBytes;
         if (in_smem) {
@@ -1186,7 +1247,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const int lo = lane * per;
       const int hi = lo + per < p.B ? lo + per : p.B;
       int sum = 0;
-      for (int b = lo; b < hi; ++b) sum += ceil_div(lens[b], kPlanTile);
+      for (int b = lo; b < hi; ++b) sum += (int)pair_units(ceil_div(lens[b], kPlanTile), kPieceUnits);
       int incl = sum;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -1196,7 +1257,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       int run = incl - sum;
       for (int b = lo; b < hi; ++b) {
         pre[b] = run;
-        run += ceil_div(lens[b], kPlanTile);
+        run += (int)pair_units(ceil_div(lens[b], kPlanTile), kPieceUnits);
       }
       if (lane == 31) pre[p.B] = incl;
     }

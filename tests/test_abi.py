@@ -175,11 +175,33 @@ def _check_balanced(B, Hq, Hkv, lens, max_len, grid, kv_dtype="bf16"):
                 assert a1 == b0 and c1 == c0 + 1
             assert all(r[3] == len(runs) for r in runs)
     assert len(slots) == 0 or max(slots) <= grid + B * hv - 2
-    # balance: every CTA gets floor or ceil of the mean number of tiles
+    # Balance by cost: pairs are laid end to end on a line of cost units, each costing
+    # 5 units (one more piece for a CTA; 0 when no lengths are given, every sequence
+    # being as long as the others) then 4 per tile; CTA i of G = min(grid, U // 4)
+    # owns the units [floor(i U / G), floor((i + 1) U / G)), so every CTA gets the same cost
+    # to a tile.  Each tile must sit in the CTA owning its unit position.
     total = sum(-(-x // 128) for x in L) * hv
     if total:
         assert tiles_per_cta.sum() == total
-        assert tiles_per_cta.max() - tiles_per_cta.min() <= 1
+        units, start = 0, {}
+        for b in range(B):
+            nt = -(-L[b] // 128)
+            for vkv in range(hv):
+                start[b, vkv] = units
+                units += (5 if lens is not None else 0) + 4 * nt if nt else 0
+        G = min(grid, units // 4)
+        owner = {}
+        for (b, vkv), runs in cover.items():
+            for lo, hi, cta, _ in runs:
+                for t in range(lo // 128, -(-hi // 128)):
+                    owner[b, vkv, t] = cta
+        for (b, vkv, t), cta in owner.items():
+            u = start[b, vkv] + (5 if lens is not None else 0) + 4 * t
+            assert cta == ((u + 1) * G - 1) // units, (b, vkv, t, cta)
+        cost = np.zeros(G)
+        for i in range(G):
+            cost[i] = (i + 1) * units // G - i * units // G
+        assert cost.max() - cost.min() <= 1
 
 
 @pytest.mark.parametrize("seed", range(12))

@@ -2,9 +2,9 @@
 
 Every mbarrier wait in the split kernel gives up after a time limit, records
 FD_ERR_TIMEOUT in the workspace error word, lets its own copies land and exits.
-The testing hook ``fd_debug_stall`` makes one CTA's producer skip one stage's
-copies (nothing is issued for it, so nothing is left in flight) and shortens the
-limit to 1 ms: the consumers' wait on that stage runs out.  The call must report
+The testing hook ``fd_debug_stall`` makes every CTA's producer skip the copies of
+one stage (nothing is issued for it, so nothing is left in flight) and shortens
+the limit to 1 ms: the consumers' waits on that stage run out.  The call must report
 FD_ERR_TIMEOUT, and the next call on the same workspace must run clean and match
 the oracle.
 """
@@ -28,7 +28,7 @@ def test_wait_that_runs_out_is_reported_and_the_next_call_is_clean(n_splits, sta
     ws = fd.Workspace()
     lib = fd.load_library()
     try:
-        lib.fd_debug_stall(stage, 1_000_000)  # skip one stage of the first CTA; waits give up after 1 ms
+        lib.fd_debug_stall(stage, 1_000_000)  # skip one stage in every CTA; waits give up after 1 ms
         run(case, n_splits=n_splits, workspace=ws)
         assert fd.workspace_status(ws) == fdb.FD_ERR_TIMEOUT
     finally:
