@@ -140,7 +140,11 @@ struct SplitCfg {
   static constexpr int kQBytes = G * D * 4;
   static constexpr int kUOff = kQOff + kQBufs * kQBytes;
   static constexpr int kPBytes = kMma ? 0 : kWarps * 32 * G * 8;  // CUDA-core engine's p rows
-  static constexpr int kObBytes = kWarps * kPubHeads * D * 4;
+  // Warp states are published in rows of kObStride floats: the padding keeps
+  // the MMA engines' float2 stores (eight heads of one warp at a time) off
+  // each other's banks.
+  static constexpr int kObStride = D + 8;
+  static constexpr int kObBytes = kWarps * kPubHeads * kObStride * 4;
   static constexpr int kWsBytes = kWarps * 128 * 4;  // merge_head weight scratch (fused merge)
   static constexpr int kUBytes0 = kPBytes > kObBytes ? kPBytes : kObBytes;
   static constexpr int kUBytes = kUBytes0 > kWsBytes ? kUBytes0 : kWsBytes;
@@ -605,9 +609,9 @@ __device__ __forceinline__ void merge_pair_smem(const SplitParams& p, uint8_t* s
   constexpr int D = C::D, EPL = D / 32, W = C::kWarps, kCons = W * 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float* so = reinterpret_cast<float*>(smem);  // [n_states, D]
-  float* sm = so + (size_t)n_states * D;       // [n_states]
-  float* sl = sm + n_states;                   // [n_states]
-  float* sw = sl + n_states;                   // [nh, 128] weights
+  float* sm = so + (size_t)n_states * D;       // [nh, 128]: m of head h, split k at h*128 + k
+  float* sl = sm + nh * 128;                   // [nh, 128]: l likewise
+  float* sw = sl + nh * 128;                   // [nh, 128] weights
   float* shead = sw + nh * 128;                // [nh, 2] (max, L)
   const uint32_t obytes = (uint32_t)n_states * D * 4;
   if (tid == 0) {
@@ -619,9 +623,13 @@ __device__ __forceinline__ void merge_pair_smem(const SplitParams& p, uint8_t* s
     for (uint32_t off = 0; off < obytes; off += kChunk)
       bulk_load(reinterpret_cast<uint8_t*>(so) + off, src + off, obytes - off < kChunk ? obytes - off : kChunk, mbar);
   }
-  for (int i = tid; i < n_states; i += kCons) {
-    sm[i] = __ldcg(p.m_part + base0 + i);
-    sl[i] = __ldcg(p.l_part + base0 + i);
+  // (m, l) land as [head][split], so that a warp reading one head's splits
+  // hits consecutive banks (the partials keep the heads of a split together).
+  for (int i = tid; i < nh * count; i += kCons) {
+    const int h = i / count, k = i - h * count;
+    const size_t g = base0 + (size_t)h * hs + (size_t)k * stride;
+    sm[h * 128 + k] = __ldcg(p.m_part + g);
+    sl[h * 128 + k] = __ldcg(p.l_part + g);
   }
   named_barrier(1, kCons);
   for (int h = warp; h < nh; h += W) {
@@ -632,8 +640,8 @@ __device__ __forceinline__ void merge_pair_smem(const SplitParams& p, uint8_t* s
       mk[r] = -INFINITY;
       lk[r] = 0.f;
       if (k < count) {
-        mk[r] = sm[h * hs + k * stride];
-        lk[r] = sl[h * hs + k * stride];
+        mk[r] = sm[h * 128 + k];
+        lk[r] = sl[h * 128 + k];
       }
     }
     const float mx = warp_max(merge_max(mk, lk));
@@ -891,7 +899,7 @@ struct CoreEngine {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const float lw = warp_sum(l[h]);
-      float* dst = obuf + (warp * G + h) * D + lane * EPL;
+      float* dst = obuf + (warp * G + h) * C::kObStride + lane * EPL;
 #pragma unroll
       for (int i = 0; i < EPL / 2; ++i) reinterpret_cast<float2*>(dst)[i] = o[h][i];
       if (lane == 0) {
@@ -1112,7 +1120,8 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
         // an empty warp state has weight 0 and O = 0, and fmaf(0, 0, a) == a
         float acc = 0.f;
 #pragma unroll
-        for (int w = 0; w < W; ++w) acc = fmaf(mlbuf[(w * PH + hl) * 2], obuf[(w * PH + hl) * D + d], acc);
+        for (int w = 0; w < W; ++w)
+          acc = fmaf(mlbuf[(w * PH + hl) * 2], obuf[(w * PH + hl) * C::kObStride + d], acc);
         if (final_here) {
           const float L = fin[hl * 2 + 1];
           p.out[((size_t)pc.b * p.Hq + head0 + h) * D + d] = M == -INFINITY ? 0.f : acc / L;
@@ -1161,7 +1170,7 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
         // With no piece after this one, the ring is idle: merge out of shared memory.
         const int n_states = balanced ? count * G : nh * count;
         const bool in_smem = C::kMma && !more && !*abort_flag && count <= kMergeKR * 32 &&
-                             (size_t)n_states * (D + 2) * 4 + (size_t)nh * 130 * 4 <=
+                             (size_t)n_states * D * 4 + (size_t)nh * (4 * 128 + 2) * 4 <=
                                  (size_t)C::kStages * C::kStageBytes;
         if (in_smem) {
           merge_pair_smem<C>(p, smem, full + 2 * C::kStages + 4, base0, n_states, count, nh, (int)hs, (int)stride,

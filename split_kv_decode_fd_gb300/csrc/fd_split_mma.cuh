@@ -228,7 +228,7 @@ struct MmaEngine {
     float ls = l + __shfl_xor_sync(0xffffffffu, l, 1);
     ls += __shfl_xor_sync(0xffffffffu, ls, 2);
     if (g >= G) return;  // idle rows
-    float* row = obuf + (warp * G + g) * D + 2 * t;
+    float* row = obuf + (warp * G + g) * C::kObStride + 2 * t;
 #pragma unroll
     for (int n = 0; n < NT; ++n)
       *reinterpret_cast<float2*>(row + 8 * n) = make_float2((o[n][0] + o[n][2]) * f, (o[n][1] + o[n][3]) * f);
@@ -429,7 +429,7 @@ struct MmaEngine16 {
     const float f = mi == -INFINITY ? 0.f : exp2f(mi - mti);
     float ls = li + __shfl_xor_sync(0xffffffffu, li, 1);
     ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-    float* row = obuf + (warp * 8 + g) * D + 2 * t;
+    float* row = obuf + (warp * 8 + g) * C::kObStride + 2 * t;
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
       const float a = hi ? o[n][2] : o[n][0];
