@@ -52,8 +52,9 @@ def parse_args():
                     help="time fd_split_partial with S splits + fd_combine (two launches per step)")
     ap.add_argument("--rows", type=int, default=1,
                     help="query rows per sequence (causal window through fd_decode_rows); 1 = fd_decode")
-    ap.add_argument("--no-graph", action="store_true",
-                    help="time K plain stream launches instead of one CUDA graph of K launches")
+    ap.add_argument("--graph", action="store_true",
+                    help="time one CUDA graph of K launches instead of K stream launches (the stream launches "
+                         "are enqueued while a short sleep kernel holds the GPU before the start event)")
     ap.add_argument("--prefill", type=int, default=0, metavar="N",
                     help="time fd_prefill on an N-token causal prompt (B=1, Hq=32, Hkv=8, D=128): TFLOP/s")
     ap.add_argument("--prefill-kv-heads", type=int, default=8, metavar="HKV",
@@ -427,11 +428,13 @@ def run_fdecode(args):
     torch.cuda.synchronize()
     launch_us = [a.elapsed_time(b) * 1e3 for a, b in ev]
 
-    # ---- timed region: K steps back to back (one CUDA graph of K launches unless --no-graph),
-    # CUDA events on the launching stream around the whole region, clocks sampled meanwhile
+    # ---- timed region: K steps back to back, CUDA events on the launching stream around the whole
+    # region, clocks sampled meanwhile.  By default K stream launches, enqueued while a sleep kernel
+    # holds the GPU before the start event (host launch latency stays outside the region and
+    # consecutive launches overlap through programmatic dependent launch); --graph: one CUDA graph.
     K = args.steps
     graph = None
-    if not args.no_graph:
+    if args.graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for _ in range(K):
@@ -448,6 +451,8 @@ def run_fdecode(args):
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    if graph is None:
+        torch.cuda._sleep(4_000_000)  # ~2 ms at 2 GHz, before the start event: the launches queue up meanwhile
     start.record(stream)
     if graph is not None:
         graph.replay()
@@ -587,7 +592,7 @@ def run_fdecode(args):
                    "kernel": f"fd_split_kernel<D={spec.D},{spec.kv_dtype},G={gpad}> (fused LSE merge)",
                    "launch": ("single launches after an L2 flush, events around each" if warm is not None else
                               "one CUDA graph of K fd_decode-family calls" if graph is not None else
-                              "K stream launches"),
+                              "K stream launches, enqueued behind a sleep kernel before the start event"),
                    "single_launch_event_us_p10_p50_p90": [round(x, 2) for x in
                                                           statistics.quantiles(launch_us, n=10)[0::4]]},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
