@@ -785,6 +785,7 @@ __device__ __forceinline__ void pv_rows(uint32_t vbase, const uint32_t* voff, ui
 template <class C>
 struct CoreEngine {
   static constexpr int G = C::G, D = C::D, EPL = C::kEPL;
+  static constexpr bool kQInSmem = false;
   float m[G], l[G];
   float2 o[G][EPL / 2];
   int32_t lim[G];  // keys each head's row may see (the piece's row limits)
@@ -1054,6 +1055,7 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
       const RowLimits rl{head0, nh, pc.len, p.n_q, p.causal};
       eng.begin(qaddr, p.qk_scale, rl);
     }
+    if constexpr (E::kQInSmem) named_barrier(1, kCons);  // every warp's share of the fragments is written
     if constexpr (C::kWide) {
       // q (if any) is in registers now and the piece is read: hand the slot back (one arrival per warp)
       __syncwarp();

@@ -78,6 +78,7 @@ struct MmaEngine {
   static constexpr int G = C::G;
   static_assert((G == 4 || G == 8) && C::kBf16 && C::kBT == 128 && C::kWarps == 4, "MMA engine layout");
 
+  static constexpr bool kQInSmem = false;
   uint32_t qa[KS][4];  // A fragments of q (hi rows 0-7, lo rows 8-15) for each k-step
   float o[NT][4];      // p.V accumulators: [.][0..1] from p_hi, [.][2..3] from p_lo
   float m, mt, l;      // head g of this lane's quad: reference max, true max, partial sum of p
@@ -254,15 +255,18 @@ struct MmaEngine16 {
   static constexpr int kRowStride = 128;
   static constexpr int kBlk = C::kBT * 128;
   static_assert(C::G == 16 && C::kBf16 && C::kBT == 128 && C::kWarps == 4, "MMA-16 engine layout");
+  static_assert(KS % 4 == 0 && KS * 1024 <= C::kUBytes, "q fragments fit the publish buffer");
 
-  uint32_t qh[KS][4], ql[KS][4];  // A fragments of q: hi and lo parts, rows = heads 0-15
+  static constexpr bool kQInSmem = true;  // begin() writes q's fragments to shared memory
   float o[NT][4];                 // p.V accumulators: [.][0..1] head g, [.][2..3] head g + 8
   float m[2], mt[2], l[2];        // heads g, g + 8: reference max, true max, partial sum
   int32_t lim[2];                 // keys each of the two heads' rows may see
+  int32_t lim_w;                  // the least row limit of the piece's live heads, over the warp
   int warp, lane, g, t;
   uint32_t kb[2], vb[2];  // ldmatrix row addresses (K, V transposed)
   uint32_t kx, vx;        // this lane's swizzle term of the 16-byte chunk index, times 16
   uint32_t zoff;
+  uint32_t fb;            // q's A fragments in shared memory: [k-step][hi, lo][lane] x 16 bytes
 
   // Byte offset of 16-byte chunk pair `c` (k-step or d-pair index) within a
   // swizzled row: chunk 2c + (lane bit) of block c / 4, XOR-swizzled by row.
@@ -270,7 +274,7 @@ struct MmaEngine16 {
     return (uint32_t)(c >> 2) * kBlk + (((uint32_t)(2 * (c & 3)) << 4) ^ x);
   }
 
-  __device__ __forceinline__ void setup(int warp_, int lane_, uint8_t*) {
+  __device__ __forceinline__ void setup(int warp_, int lane_, uint8_t* smem) {
     warp = warp_;
     lane = lane_;
     g = lane >> 2;
@@ -286,6 +290,7 @@ struct MmaEngine16 {
     vx = (uint32_t)((mi >> 1) ^ r) << 4;
     const int zb = lane * (D / 16);
     zoff = (zb / 128) * kBlk + (zb % 128);
+    fb = smem_addr(smem) + C::kUOff;
   }
 
   __device__ __forceinline__ void reset() {
@@ -301,23 +306,58 @@ struct MmaEngine16 {
       for (int j = 0; j < 4; ++j) o[n][j] = 0.f;
   }
 
+  // q rows of the piece (fp32 in shared memory), times scale*log2(e), split
+  // hi/lo into the A fragments of every k-step; the four warps convert a
+  // quarter each into the publish buffer, idle until the piece ends.  The
+  // caller's barrier after begin() makes all of them visible.
   __device__ __forceinline__ void begin(uint32_t qaddr, float qk_scale, const RowLimits& rl) {
     lim[0] = rl(g);
     lim[1] = rl(g + 8);
+    // heads past the piece's live ones (lim 0) are never published: no bound for them
+    int32_t lw = min(g < rl.nh ? lim[0] : 0x7fffffff, g + 8 < rl.nh ? lim[1] : 0x7fffffff);
 #pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
+    for (int o = 1; o < 32; o <<= 1) lw = min(lw, __shfl_xor_sync(0xffffffffu, lw, o));
+    lim_w = lw;
+#pragma unroll
+    for (int j = 0; j < KS / 4; ++j) {
+      const int kk = warp * (KS / 4) + j;
       const uint32_t a = qaddr + (g * D + 16 * kk + 2 * t) * 4;
       const uint32_t b = a + 8 * D * 4;  // row g + 8
       const float2 x0 = lds64f(a), x1 = lds64f(a + 32);
       const float2 y0 = lds64f(b), y1 = lds64f(b + 32);
-      split_bf16x2(x0.x * qk_scale, x0.y * qk_scale, qh[kk][0], ql[kk][0]);  // row g,     k 2t..
-      split_bf16x2(y0.x * qk_scale, y0.y * qk_scale, qh[kk][1], ql[kk][1]);  // row g + 8, k 2t..
-      split_bf16x2(x1.x * qk_scale, x1.y * qk_scale, qh[kk][2], ql[kk][2]);  // row g,     k 2t+8..
-      split_bf16x2(y1.x * qk_scale, y1.y * qk_scale, qh[kk][3], ql[kk][3]);  // row g + 8, k 2t+8..
+      uint32_t h[4], l[4];
+      split_bf16x2(x0.x * qk_scale, x0.y * qk_scale, h[0], l[0]);  // row g,     k 2t..
+      split_bf16x2(y0.x * qk_scale, y0.y * qk_scale, h[1], l[1]);  // row g + 8, k 2t..
+      split_bf16x2(x1.x * qk_scale, x1.y * qk_scale, h[2], l[2]);  // row g,     k 2t+8..
+      split_bf16x2(y1.x * qk_scale, y1.y * qk_scale, h[3], l[3]);  // row g + 8, k 2t+8..
+      const uint32_t f = fb + (uint32_t)kk * 1024 + lane * 16;
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(f), "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                   : "memory");
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(f + 512), "r"(l[0]), "r"(l[1]), "r"(l[2]),
+                   "r"(l[3])
+                   : "memory");
     }
   }
 
+  __device__ __forceinline__ void qfrag(int kk, uint32_t (&h)[4], uint32_t (&l)[4]) const {
+    const uint32_t f = fb + (uint32_t)kk * 1024 + lane * 16;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+                 : "r"(f));
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(l[0]), "=r"(l[1]), "=r"(l[2]), "=r"(l[3])
+                 : "r"(f + 512));
+  }
+
   __device__ __forceinline__ void tile(uint32_t kst, uint32_t vst, int nv, uint32_t, float, int32_t tok0) {
+    // A full stage that no head's row limit cuts (every stage but the last of
+    // a piece) takes the straight-line path: no masks and no branches but the
+    // rare rescale, so the compiler can overlap one key half's softmax with
+    // the other half's MMAs.
+    if (nv == 32 && tok0 + 32 * warp + 32 <= lim_w) {
+      tile_impl<true>(kst, vst, 32, tok0);
+      return;
+    }
     if (nv < 32) {
       // Rows past the valid keys get p = 0, but 0 * NaN is NaN: clear those V rows.
       for (int r = nv; r < 32; ++r) {
@@ -330,27 +370,36 @@ struct MmaEngine16 {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
     }
-    const bool two = nv > 16;
-    // ---- q.k: hi and lo parts accumulate into the same registers
-    float sc[4][4];
+    tile_impl<false>(kst, vst, nv, tok0);
+  }
+
+  template <bool kFull>
+  __device__ __forceinline__ void tile_impl(uint32_t kst, uint32_t vst, int nv, int32_t tok0) {
+    const bool two = kFull || nv > 16;
+    // ---- q.k: q_hi.k and q_lo.k in separate accumulators (independent MMA chains)
+    float sc[4][4], sl[4][4];
 #pragma unroll
     for (int n = 0; n < 4; ++n)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) sc[n][j] = 0.f;
+      for (int j = 0; j < 4; ++j) sc[n][j] = sl[n][j] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
-      uint32_t b0, b1, b2, b3;
+      uint32_t qh[4], ql[4];
+      qfrag(kk, qh, ql);
+      uint32_t b0, b1, b2, b3, c0 = 0, c1 = 0, c2 = 0, c3 = 0;
       ldsm_x4(kst + kb[0] + chunk_off(kk, kx), b0, b1, b2, b3);
-      mma_bf16_16816(sc[0], qh[kk], b0, b1);
-      mma_bf16_16816(sc[1], qh[kk], b2, b3);
-      mma_bf16_16816(sc[0], ql[kk], b0, b1);
-      mma_bf16_16816(sc[1], ql[kk], b2, b3);
+      if (two) ldsm_x4(kst + kb[1] + chunk_off(kk, kx), c0, c1, c2, c3);
+      mma_bf16_16816(sc[0], qh, b0, b1);
+      mma_bf16_16816(sc[1], qh, b2, b3);
       if (two) {
-        ldsm_x4(kst + kb[1] + chunk_off(kk, kx), b0, b1, b2, b3);
-        mma_bf16_16816(sc[2], qh[kk], b0, b1);
-        mma_bf16_16816(sc[3], qh[kk], b2, b3);
-        mma_bf16_16816(sc[2], ql[kk], b0, b1);
-        mma_bf16_16816(sc[3], ql[kk], b2, b3);
+        mma_bf16_16816(sc[2], qh, c0, c1);
+        mma_bf16_16816(sc[3], qh, c2, c3);
+      }
+      mma_bf16_16816(sl[0], ql, b0, b1);
+      mma_bf16_16816(sl[1], ql, b2, b3);
+      if (two) {
+        mma_bf16_16816(sl[2], ql, c0, c1);
+        mma_bf16_16816(sl[3], ql, c2, c3);
       }
     }
     // ---- online softmax, heads g (i = 0) and g + 8 (i = 1)
@@ -365,7 +414,8 @@ struct MmaEngine16 {
         const int32_t tok = tok0 + 32 * warp + key;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-          s[i][n][j] = (in && tok < lim[i]) ? sc[n][2 * i + j] : -INFINITY;
+          const float v = sc[n][2 * i + j] + sl[n][2 * i + j];
+          s[i][n][j] = (kFull || (in && tok < lim[i])) ? v : -INFINITY;
           smax[i] = fmaxf(smax[i], s[i][n][j]);
         }
       }
@@ -389,32 +439,34 @@ struct MmaEngine16 {
       // a head whose row has seen no key yet (m = -inf) gets p = 0 for every key
       mref[i] = m[i] == -INFINITY ? 0.f : m[i];
     }
-    // p as A fragments: a0 = (row g, keys 2t..), a1 = (row g+8, keys 2t..),
-    // a2 = (row g, keys 2t+8..), a3 = (row g+8, keys 2t+8..) of each 16-key chunk
-    uint32_t ph[2][4], pl[2][4];
+    // ---- per 16-key half: p as A fragments, then p.V.  a0 = (row g, keys
+    // 2t..), a1 = (row g+8, keys 2t..), a2 = (row g, keys 2t+8..), a3 = (row
+    // g+8, keys 2t+8..) of the half.
 #pragma unroll
     for (int j2 = 0; j2 < 2; ++j2) {
+      if (j2 == 1 && !two) break;
+      uint32_t ph[4], pl[4];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const float p0 = exp2f(s[i][2 * j2][0] - mref[i]), p1 = exp2f(s[i][2 * j2][1] - mref[i]);
         const float p2 = exp2f(s[i][2 * j2 + 1][0] - mref[i]), p3 = exp2f(s[i][2 * j2 + 1][1] - mref[i]);
         l[i] += (p0 + p1) + (p2 + p3);
-        split_bf16x2(p0, p1, ph[j2][i], pl[j2][i]);
-        split_bf16x2(p2, p3, ph[j2][2 + i], pl[j2][2 + i]);
+        split_bf16x2(p0, p1, ph[i], pl[i]);
+        split_bf16x2(p2, p3, ph[2 + i], pl[2 + i]);
       }
-    }
-    // ---- p.V
 #pragma unroll
-    for (int j2 = 0; j2 < 2; ++j2) {
-      if (j2 == 1 && !two) break;
-#pragma unroll
-      for (int np = 0; np < NT / 2; ++np) {
-        uint32_t b0, b1, b2, b3;
+      for (int np = 0; np < NT / 2; np += 2) {
+        uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
         ldsm_x4_t(vst + vb[j2] + chunk_off(np, vx), b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * np], ph[j2], b0, b1);
-        mma_bf16_16816(o[2 * np + 1], ph[j2], b2, b3);
-        mma_bf16_16816(o[2 * np], pl[j2], b0, b1);
-        mma_bf16_16816(o[2 * np + 1], pl[j2], b2, b3);
+        ldsm_x4_t(vst + vb[j2] + chunk_off(np + 1, vx), c0, c1, c2, c3);
+        mma_bf16_16816(o[2 * np], ph, b0, b1);
+        mma_bf16_16816(o[2 * np + 1], ph, b2, b3);
+        mma_bf16_16816(o[2 * np + 2], ph, c0, c1);
+        mma_bf16_16816(o[2 * np + 3], ph, c2, c3);
+        mma_bf16_16816(o[2 * np], pl, b0, b1);
+        mma_bf16_16816(o[2 * np + 1], pl, b2, b3);
+        mma_bf16_16816(o[2 * np + 2], pl, c0, c1);
+        mma_bf16_16816(o[2 * np + 3], pl, c2, c3);
       }
     }
   }
