@@ -153,7 +153,7 @@ struct SplitCfg {
   static constexpr int kLenOff = kFinOff + kPubHeads * 8;
   static constexpr int kPreOff = kLenOff + (kAutoMaxBatch + 4) * 4;
   static constexpr int kBarOff = kPreOff + (kAutoMaxBatch + 4) * 4;
-  static constexpr int kFlagOff = kBarOff + (2 * kStages + 5) * 8;
+  static constexpr int kFlagOff = kBarOff + (2 * kStages + 6) * 8;
   static constexpr int kDescOff = (kFlagOff + 16 + 15) / 16 * 16;  // PieceDesc per q slot
   static constexpr int kBytes = kDescOff + 2 * 48;
   static constexpr int kSmemAlloc = kBytes + 1024;
@@ -595,99 +595,176 @@ __device__ __forceinline__ void producer_warp(const CUtensorMap* tk, const CUten
 
 // The last arriver's merge of a whole (b, virtual KV head), for a CTA with no
 // piece after this one: its K/V ring is idle, so the pair's partial outputs
-// come into it with one bulk copy (one round trip to L2 for all heads and
-// splits) while the threads load every (m, l) beside it; the weights and the
-// weighted sums then run out of shared memory.  The arithmetic per output
-// element is merge_head's (same weights, same four interleaved partial sums in
-// increasing k, same final division), so both give identical bits.
+// come into it with bulk copies (one round trip to L2 for all heads and
+// splits), and the (m, l) of every state with a small copy of their own on a
+// second barrier, so that the weights are ready while the outputs still land;
+// the weighted sums then run out of shared memory, every thread's outputs
+// summed in one interleaved pass.  The arithmetic per output element is
+// merge_head's (same weights, same four interleaved partial sums in increasing
+// k, same final division), so both give identical bits.
 // State (h, k) of the pair is partial index base0 + h*hs + k*stride; all
 // n_states indices lie in [base0, base0 + n_states).  count <= 128.
 template <class C>
-__device__ __forceinline__ void merge_pair_smem(const SplitParams& p, uint8_t* smem, uint64_t* mbar, size_t base0,
-                                                int n_states, int count, int nh, int hs, int stride, float* out_rows,
-                                                float* lse_slots) {
+__device__ __forceinline__ void merge_pair_smem(const SplitParams& p, uint8_t* smem, uint64_t* mbar_o,
+                                                uint64_t* mbar_ml, size_t base0, int n_states, int count, int nh,
+                                                int hs, int stride, float* out_rows, float* lse_slots) {
   constexpr int D = C::D, EPL = D / 32, W = C::kWarps, kCons = W * 32;
+  constexpr int HPW = (C::G + W - 1) / W;          // heads per warp in the weights
+  constexpr int IPT = (C::G * 32 + kCons - 1) / kCons;  // (head, lane slice) items per thread in the sums
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ns4 = (n_states + 3) & ~3;         // keeps every array below 16-byte aligned
   float* so = reinterpret_cast<float*>(smem);  // [n_states, D]
-  float* sm = so + (size_t)n_states * D;       // [nh, 128]: m of head h, split k at h*128 + k
-  float* sl = sm + nh * 128;                   // [nh, 128]: l likewise
-  float* sw = sl + nh * 128;                   // [nh, 128] weights
+  float* rm = so + (size_t)n_states * D;       // [n_states] m of every state, in partial order
+  float* rl = rm + ns4;                        // [n_states] l likewise
+  float* sw = rl + ns4;                        // [nh, 128] weights: head h, split k at h*128 + k
   float* shead = sw + nh * 128;                // [nh, 2] (max, L)
   const uint32_t obytes = (uint32_t)n_states * D * 4;
+  const uint32_t mlbytes = (uint32_t)n_states * 4;
+  const float* gm = p.m_part + base0;
+  const float* gl = p.l_part + base0;
+  const bool ml_bulk = (mlbytes & 15) == 0 && ((reinterpret_cast<uintptr_t>(gm) | reinterpret_cast<uintptr_t>(gl)) & 15) == 0;
   if (tid == 0) {
     // the ring's reads by the consumers (generic proxy) come before these async-proxy writes
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_arrive_expect_tx(mbar, obytes);
+    if (ml_bulk) {
+      mbar_arrive_expect_tx(mbar_ml, 2 * mlbytes);
+      bulk_load(reinterpret_cast<uint8_t*>(rm), gm, mlbytes, mbar_ml);
+      bulk_load(reinterpret_cast<uint8_t*>(rl), gl, mlbytes, mbar_ml);
+    }
+    mbar_arrive_expect_tx(mbar_o, obytes);
     const uint8_t* src = reinterpret_cast<const uint8_t*>(p.o_part + base0 * D);
     constexpr uint32_t kChunk = 32768;
     for (uint32_t off = 0; off < obytes; off += kChunk)
-      bulk_load(reinterpret_cast<uint8_t*>(so) + off, src + off, obytes - off < kChunk ? obytes - off : kChunk, mbar);
+      bulk_load(reinterpret_cast<uint8_t*>(so) + off, src + off, obytes - off < kChunk ? obytes - off : kChunk, mbar_o);
   }
-  // (m, l) land as [head][split], so that a warp reading one head's splits
-  // hits consecutive banks (the partials keep the heads of a split together).
-  for (int i = tid; i < nh * count; i += kCons) {
-    const int h = i / count, k = i - h * count;
-    const size_t g = base0 + (size_t)h * hs + (size_t)k * stride;
-    sm[h * 128 + k] = __ldcg(p.m_part + g);
-    sl[h * 128 + k] = __ldcg(p.l_part + g);
-  }
-  named_barrier(1, kCons);
-  for (int h = warp; h < nh; h += W) {
-    float mk[kMergeKR], lk[kMergeKR], wk[kMergeKR];
+  bool ok = true;
+  if (ml_bulk) {
+    ok = mbar_wait_for(mbar_ml, 0, wait_limit(p));
+  } else {
+    for (int i0 = 0; i0 < n_states; i0 += 4 * kCons) {
+      float mv[4], lv[4];
 #pragma unroll
-    for (int r = 0; r < kMergeKR; ++r) {
-      const int k = r * 32 + lane;
-      mk[r] = -INFINITY;
-      lk[r] = 0.f;
-      if (k < count) {
-        mk[r] = sm[h * 128 + k];
-        lk[r] = sl[h * 128 + k];
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kCons + tid;
+        mv[u] = i < n_states ? __ldcg(gm + i) : 0.f;
+        lv[u] = i < n_states ? __ldcg(gl + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kCons + tid;
+        if (i < n_states) {
+          rm[i] = mv[u];
+          rl[i] = lv[u];
+        }
       }
     }
-    const float mx = warp_max(merge_max(mk, lk));
-    float L = 0.f;
-    if (mx != -INFINITY) {
-      L = warp_sum(merge_weights(mk, lk, mx, wk));
-    } else {
+    named_barrier(1, kCons);
+  }
+  if (!ok) {
+    raise_error(p.err, kErrTimeout);
+    mbar_wait_for(mbar_ml, 0, wait_limit(p));  // give the copy its chance to land before the CTA leaves
+  }
+  if (count <= 32) {
+    // One split per lane: the warp's heads reduce together (merge_max,
+    // merge_weights and the warp reductions of merge_head, interleaved).
+    float mk[HPW], lk[HPW], mx[HPW], wk[HPW], ls[HPW];
 #pragma unroll
-      for (int r = 0; r < kMergeKR; ++r) wk[r] = 0.f;
+    for (int i = 0; i < HPW; ++i) {
+      const int h = warp + i * W;
+      mk[i] = -INFINITY;
+      lk[i] = 0.f;
+      if (h < nh && lane < count) {
+        mk[i] = rm[h * hs + lane * stride];
+        lk[i] = rl[h * hs + lane * stride];
+      }
+      mx[i] = lk[i] > 0.f ? mk[i] : -INFINITY;
     }
 #pragma unroll
-    for (int r = 0; r < kMergeKR; ++r) sw[h * 128 + r * 32 + lane] = wk[r];
-    if (lane == 0) {
-      shead[2 * h] = mx;
-      shead[2 * h + 1] = L;
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int i = 0; i < HPW; ++i) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], o));
+#pragma unroll
+    for (int i = 0; i < HPW; ++i) {
+      wk[i] = (mx[i] != -INFINITY && lk[i] > 0.f) ? exp2f((mk[i] - mx[i]) * kLog2e) : 0.f;
+      ls[i] = fmaf(wk[i], lk[i], 0.f);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int i = 0; i < HPW; ++i) ls[i] += __shfl_xor_sync(0xffffffffu, ls[i], o);
+#pragma unroll
+    for (int i = 0; i < HPW; ++i) {
+      const int h = warp + i * W;
+      if (h < nh) {
+        sw[h * 128 + lane] = wk[i];
+        if (lane == 0) {
+          shead[2 * h] = mx[i];
+          shead[2 * h + 1] = mx[i] == -INFINITY ? 0.f : ls[i];
+        }
+      }
+    }
+  } else {
+    for (int h = warp; h < nh; h += W) {
+      float mk[kMergeKR], lk[kMergeKR], wk[kMergeKR];
+#pragma unroll
+      for (int r = 0; r < kMergeKR; ++r) {
+        const int k = r * 32 + lane;
+        mk[r] = -INFINITY;
+        lk[r] = 0.f;
+        if (k < count) {
+          mk[r] = rm[h * hs + k * stride];
+          lk[r] = rl[h * hs + k * stride];
+        }
+      }
+      const float mx = warp_max(merge_max(mk, lk));
+      float L = 0.f;
+      if (mx != -INFINITY) {
+        L = warp_sum(merge_weights(mk, lk, mx, wk));
+      } else {
+#pragma unroll
+        for (int r = 0; r < kMergeKR; ++r) wk[r] = 0.f;
+      }
+#pragma unroll
+      for (int r = 0; r < kMergeKR; ++r) sw[h * 128 + r * 32 + lane] = wk[r];
+      if (lane == 0) {
+        shead[2 * h] = mx;
+        shead[2 * h + 1] = L;
+      }
     }
   }
-  if (!mbar_wait_for(mbar, 0, wait_limit(p))) {
+  if (!mbar_wait_for(mbar_o, 0, wait_limit(p))) {
     raise_error(p.err, kErrTimeout);
-    mbar_wait_for(mbar, 0, wait_limit(p));  // give the copy its chance to land before the CTA leaves
+    mbar_wait_for(mbar_o, 0, wait_limit(p));  // give the copy its chance to land before the CTA leaves
   }
   named_barrier(1, kCons);
-  for (int item = tid; item < nh * 32; item += kCons) {
-    const int h = item >> 5, j = item & 31;
-    const float mx = shead[2 * h], L = shead[2 * h + 1];
-    float* orow = out_rows + (size_t)h * D + j * EPL;
-    if (mx == -INFINITY) {
+  // Item (h, j): head h, output elements [j*EPL, (j+1)*EPL).  Thread tid takes
+  // items tid + i*kCons, i < IPT (one head per warp and i), all at once.
+  float acc[IPT][4][EPL];
+  const float* wrow[IPT];
+  const float* obase[IPT];
+  bool live[IPT];
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) orow[e] = 0.f;
-      if (lse_slots && j == 0) lse_slots[h] = -INFINITY;
-      continue;
-    }
-    float acc[4][EPL];
+  for (int i = 0; i < IPT; ++i) {
+    const int item = tid + i * kCons;
+    const int h = item >> 5, j = item & 31;
+    live[i] = item < nh * 32 && shead[2 * (h < nh ? h : 0)] != -INFINITY;
+    wrow[i] = sw + (h < nh ? h : 0) * 128;
+    obase[i] = so + (size_t)(h < nh ? h : 0) * hs * D + j * EPL;
 #pragma unroll
     for (int s4 = 0; s4 < 4; ++s4)
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[s4][e] = 0.f;
-    const float* wrow = sw + h * 128;
-    const float* obase = so + (size_t)h * hs * D + j * EPL;
-    for (int k0 = 0; k0 < count; k0 += 4) {
+      for (int e = 0; e < EPL; ++e) acc[i][s4][e] = 0.f;
+  }
+  for (int k0 = 0; k0 < count; k0 += 4) {
+#pragma unroll
+    for (int i = 0; i < IPT; ++i) {
+      if (!live[i]) continue;
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         const int k = k0 + jj;
         if (k < count) {
-          const float w = wrow[k];
-          const float* v = obase + (size_t)k * stride * D;
+          const float w = wrow[i][k];
+          const float* v = obase[i] + (size_t)k * stride * D;
           float vv[EPL];
           if constexpr (EPL == 4) {
             const float4 x = *reinterpret_cast<const float4*>(v);
@@ -701,12 +778,26 @@ __device__ __forceinline__ void merge_pair_smem(const SplitParams& p, uint8_t* s
             vv[1] = x.y;
           }
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[jj][e] = fmaf(w, vv[e], acc[jj][e]);
+          for (int e = 0; e < EPL; ++e) acc[i][jj][e] = fmaf(w, vv[e], acc[i][jj][e]);
         }
       }
     }
+  }
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) orow[e] = (((acc[0][e] + acc[1][e]) + acc[2][e]) + acc[3][e]) / L;
+  for (int i = 0; i < IPT; ++i) {
+    const int item = tid + i * kCons;
+    if (item >= nh * 32) continue;
+    const int h = item >> 5, j = item & 31;
+    float* orow = out_rows + (size_t)h * D + j * EPL;
+    const float mx = shead[2 * h], L = shead[2 * h + 1];
+    if (mx == -INFINITY) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) orow[e] = 0.f;
+      if (lse_slots && j == 0) lse_slots[h] = -INFINITY;
+      continue;
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) orow[e] = (((acc[i][0][e] + acc[i][1][e]) + acc[i][2][e]) + acc[i][3][e]) / L;
     if (lse_slots && j == 0) lse_slots[h] = mx + logf(L);
   }
 }
@@ -1172,10 +1263,12 @@ __device__ __forceinline__ void consumer_warps(const SplitParams& p, const CtaTi
         // With no piece after this one, the ring is idle: merge out of shared memory.
         const int n_states = balanced ? count * G : nh * count;
         const bool in_smem = C::kMma && !more && !*abort_flag && count <= kMergeKR * 32 &&
-                             (size_t)n_states * D * 4 + (size_t)nh * (4 * 128 + 2) * 4 <=
+                             (size_t)n_states * D * 4 + (size_t)((n_states + 3) & ~3) * 8 +
+                                     (size_t)nh * (128 + 2) * 4 <=
                                  (size_t)C::kStages * C::kStageBytes;
         if (in_smem) {
-          merge_pair_smem<C>(p, smem, full + 2 * C::kStages + 4, base0, n_states, count, nh, (int)hs, (int)stride,
+          merge_pair_smem<C>(p, smem, full + 2 * C::kStages + 4, full + 2 * C::kStages + 5, base0, n_states, count,
+                             nh, (int)hs, (int)stride,
                              p.out + ((size_t)pc.b * p.Hq + head0) * D,
                              p.lse ? p.lse + (size_t)pc.b * p.Hq + head0 : nullptr);
         } else {
@@ -1224,7 +1317,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(bars + 2 * C::kStages + i, 1);                               // q full
       mbar_init(bars + 2 * C::kStages + 2 + i, C::kWide ? C::kWarps : 1);    // q empty
     }
-    mbar_init(bars + 2 * C::kStages + 4, 1);  // the pair merge's bulk copy (merge_pair_smem)
+    mbar_init(bars + 2 * C::kStages + 4, 1);  // the pair merge's bulk copies: partial outputs
+    mbar_init(bars + 2 * C::kStages + 5, 1);  // ... and (m, l) (merge_pair_smem)
     *abort_flag = 0;
     fence_barrier_init();
   }
