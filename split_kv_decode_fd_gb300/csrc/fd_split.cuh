@@ -740,16 +740,17 @@ __device__ __forceinline__ void merge_pair_smem(const SplitParams& p, uint8_t* s
   // Item (h, j): head h, output elements [j*EPL, (j+1)*EPL).  Thread tid takes
   // items tid + i*kCons, i < IPT (one head per warp and i), all at once.
   float acc[IPT][4][EPL];
-  const float* wrow[IPT];
-  const float* obase[IPT];
+  uint32_t wa[IPT], oa[IPT];  // shared addresses: the item's weights and its slice of split 0
   bool live[IPT];
+  const uint32_t kstep = (uint32_t)stride * D * 4;  // bytes from split k to k + 1
 #pragma unroll
   for (int i = 0; i < IPT; ++i) {
     const int item = tid + i * kCons;
     const int h = item >> 5, j = item & 31;
-    live[i] = item < nh * 32 && shead[2 * (h < nh ? h : 0)] != -INFINITY;
-    wrow[i] = sw + (h < nh ? h : 0) * 128;
-    obase[i] = so + (size_t)(h < nh ? h : 0) * hs * D + j * EPL;
+    const int hc = h < nh ? h : 0;
+    live[i] = item < nh * 32 && shead[2 * hc] != -INFINITY;
+    wa[i] = smem_addr(sw + hc * 128);
+    oa[i] = smem_addr(so) + (uint32_t)((hc * hs * D + j * EPL) * 4);
 #pragma unroll
     for (int s4 = 0; s4 < 4; ++s4)
 #pragma unroll
@@ -763,19 +764,19 @@ __device__ __forceinline__ void merge_pair_smem(const SplitParams& p, uint8_t* s
       for (int jj = 0; jj < 4; ++jj) {
         const int k = k0 + jj;
         if (k < count) {
-          const float w = wrow[i][k];
-          const float* v = obase[i] + (size_t)k * stride * D;
+          const float w = __uint_as_float(lds32u(wa[i] + 4 * k));
+          const uint32_t va = oa[i] + (uint32_t)k * kstep;
           float vv[EPL];
           if constexpr (EPL == 4) {
-            const float4 x = *reinterpret_cast<const float4*>(v);
+            const float4 x = lds128(va);
             vv[0] = x.x;
             vv[1] = x.y;
             vv[2] = x.z;
             vv[3] = x.w;
           } else {
-            const float2 x = *reinterpret_cast<const float2*>(v);
-            vv[0] = x.x;
-            vv[1] = x.y;
+            const uint2 x = lds64u(va);
+            vv[0] = __uint_as_float(x.x);
+            vv[1] = __uint_as_float(x.y);
           }
 #pragma unroll
           for (int e = 0; e < EPL; ++e) acc[i][jj][e] = fmaf(w, vv[e], acc[i][jj][e]);
