@@ -132,8 +132,18 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* addr, int v) {
 }
 
 // Barrier over a subset of warps (ids 1..15; 0 is __syncthreads).
+// bar.sync is warp-aligned: a warp counts as arrived as soon as any of its
+// lanes executes it, so each warp first gathers its lanes (a lane may still be
+// in a branch of its own, e.g. a spin-wait only lane 0 runs).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
+  __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// __syncthreads() for code where a warp's lanes may have diverged.
+__device__ __forceinline__ void cta_sync() {
+  __syncwarp();
+  __syncthreads();
 }
 
 __device__ __forceinline__ float4 lds128(uint32_t addr) {

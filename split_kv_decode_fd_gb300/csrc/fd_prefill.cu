@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
@@ -603,10 +603,10 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         // q rows, times scale*log2(e), as bf16 hi / lo in the swizzled A layout.  The
         // previous item's S MMAs are all complete (this group saw its last S).  The
         // warp loads its 32 rows together: each load instruction covers 512
-        // contiguous bytes (128 / D rows), 8 instructions in flight per batch.
+        // contiguous bytes (128 / D rows), 16 instructions in flight per batch.
         {
           constexpr int kLoads = 32 * kD / 128;  // per lane, for the warp's 32 rows
-          constexpr int kBatch = kLoads < 8 ? kLoads : 8;
+          constexpr int kBatch = kLoads < 16 ? kLoads : 16;
           const size_t head_row0 = ((size_t)it.b * p.Hq + h) * p.n_q;
 #pragma unroll 1
           for (int i0 = 0; i0 < kLoads; i0 += kBatch) {
@@ -762,7 +762,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");

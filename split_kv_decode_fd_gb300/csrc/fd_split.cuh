@@ -1346,7 +1346,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   if (p.n_splits == 0 && p.seq_lens != nullptr) {
     tl.uniform = 0;
     for (int b = tid; b < p.B; b += C::kThreads) lens[b] = clamp_len(__ldg(p.seq_lens + b) + p.append, p.max_len);
-    __syncthreads();
+    cta_sync();
     if (warp == 0) {
       const int lane = tid & 31;
       const int per = ceil_div(p.B, 32);
@@ -1369,7 +1369,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  __syncthreads();
+  cta_sync();
   const int64_t total = (int64_t)p.hv * tl.prefix(p.B);
 
   if (warp == C::kWarps)
