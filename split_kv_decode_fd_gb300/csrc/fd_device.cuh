@@ -92,6 +92,23 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return pol;
 }
 
+// Shared memory -> global through a tensor map (a bulk-group copy); rows and
+// columns outside the map's extents are not written.  The coordinates are
+// never negative here.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(src)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until every committed bulk group of this thread has finished reading its
+// shared-memory source (the source may be overwritten, or the CTA exit); the
+// global writes complete on their own, before the grid does.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // tma_load_3d with an L2 cache policy.
 __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
                                                  int32_t y, int32_t z, uint64_t policy) {
@@ -132,9 +149,9 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* addr, int v) {
 }
 
 // Barrier over a subset of warps (ids 1..15; 0 is __syncthreads).
-// bar.sync is warp-aligned: a warp counts as arrived as soon as any of its
-// lanes executes it, so each warp first gathers its lanes (a lane may still be
-// in a branch of its own, e.g. a spin-wait only lane 0 runs).
+// bar.sync is the warp-aligned form: every lane of a warp must execute the same
+// instance, so each warp first gathers its lanes (one of them may still be in a
+// branch of its own, e.g. a spin-wait that only lane 0 runs).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
   __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

@@ -25,7 +25,9 @@ constexpr int kPrefillRows = 128;
 constexpr int kPrefillKeys = 128;
 
 // D = 64 or 128; cudaErrorInvalidValue otherwise.
-cudaError_t launch_prefill(int D, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
-                           cudaStream_t stream);
+// `to`: the output [B*Hq, n_q, D] fp32, 32-column x 128-row boxes with the
+// 128-byte swizzle (the kernel's epilogue stores through it).
+cudaError_t launch_prefill(int D, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                           const PrefillParams& p, cudaStream_t stream);
 
 }  // namespace fdk

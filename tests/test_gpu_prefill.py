@@ -178,3 +178,25 @@ def test_prefill_sequences_without_keys(hq, hkv, layout):
         assert_close(np64(lse), ref_lse, "lse")
         assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
         assert torch.all(torch.isneginf(lse[0])) and torch.all(torch.isneginf(lse[2]))
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(4, 2, 128), (6, 2, 128), (4, 4, 64)],
+                         ids=["two_heads_per_cta", "one_head_per_cta", "d64_mha"])
+def test_prefill_writes_only_its_rows(hq, hkv, d):
+    """The epilogue stores 128-row tiles through a tensor map per head: the rows of
+    the last tile past n_q (here 2 of 128) must not be written, neither into the
+    next head's rows nor past the end of the output."""
+    spec = small_spec("tail_rows", 2, hq, hkv, d, 300, lengths="uniform:140:300", seed=31)
+    case = make_case(spec, "cuda")
+    n_q = 130
+    q = window_q(case, n_q, seed=13)
+    numel = spec.B * hq * n_q * d
+    big = torch.full((numel + 4096,), 12345.0, device="cuda")
+    out = big[:numel].view(spec.B, hq, n_q, d)
+    lse = torch.empty((spec.B, hq, n_q), device="cuda")
+    run_prefill(case, q, True, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(big[numel:] == 12345.0), "the prefill wrote past its output"
+    ref_out, ref_lse = oracle_rows(case, q, True)
+    assert_close(np64(out), ref_out, "out")
+    assert_close(np64(lse), ref_lse, "lse")
