@@ -198,16 +198,17 @@ fd_status make_maps(const fd_kv_desc* kv, int B, int Hkv, int D, CUtensorMap* tk
   return FD_OK;
 }
 
-// The prefill output [rows = B*Hq][n_q][D] fp32 as a tensor map: boxes of 32
+// The prefill's q or output [B*Hq][n_q][D] fp32 as a tensor map: boxes of 32
 // columns (128 bytes, the 128-byte swizzle) x 128 query rows of one head, so
-// that a tile's rows past n_q fall outside the map and are not written.
-fd_status make_out_map(float* out, int64_t heads, int32_t n_q, int32_t D, CUtensorMap* to) {
+// that a tile's rows past n_q fall outside the map: loads read zeros there,
+// stores leave them alone.
+fd_status make_rows_map(const float* base, int64_t heads, int32_t n_q, int32_t D, CUtensorMap* to) {
   auto encode = encode_fn();
   if (!encode) return FD_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)n_q, (cuuint64_t)heads};
   cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)n_q * D * 4};
   cuuint32_t box[3] = {32, (cuuint32_t)kPrefillRows, 1}, estr[3] = {1, 1, 1};
-  CUresult r = encode(to, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box, estr,
+  CUresult r = encode(to, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
@@ -477,9 +478,10 @@ fd_status fd_prefill(const float* q, int32_t n_q, int32_t causal, const fd_kv_de
   if (kv->dtype != FD_BF16) return FD_ERR_UNSUPPORTED;
   if (B > 65535 || Hq > 65535 || (int64_t)B * Hq * n_q * D > ((int64_t)1 << 40)) return FD_ERR_UNSUPPORTED;
   if ((int64_t)B * Hq > INT32_MAX) return FD_ERR_UNSUPPORTED;  // a tensor-map coordinate
-  CUtensorMap tk, tv, to;
+  CUtensorMap tk, tv, tq, to;
   if ((st = make_maps(kv, B, Hkv, D, &tk, &tv)) != FD_OK) return st;
-  if ((st = make_out_map(out, (int64_t)B * Hq, n_q, D, &to)) != FD_OK) return st;
+  if ((st = make_rows_map(q, (int64_t)B * Hq, n_q, D, &tq)) != FD_OK) return st;
+  if ((st = make_rows_map(out, (int64_t)B * Hq, n_q, D, &to)) != FD_OK) return st;
   PrefillParams p;
   std::memset(&p, 0, sizeof(p));
   p.q = q;
@@ -500,7 +502,7 @@ fd_status fd_prefill(const float* q, int32_t n_q, int32_t causal, const fd_kv_de
   p.max_pages = kv->max_pages_per_seq;
   p.num_pages = kv->num_pages;
   p.qk_scale = (float)((double)scale * 1.4426950408889634);
-  return launch_prefill(D, tk, tv, to, p, (cudaStream_t)stream) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+  return launch_prefill(D, tk, tv, tq, to, p, (cudaStream_t)stream) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
 int32_t fd_attend_backend(int32_t n_q, int32_t Hq, int32_t Hkv, int32_t D, int32_t kv_dtype) {

@@ -329,7 +329,8 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int32_t idx, int
 template <int D, int NG>
 __global__ void __launch_bounds__(kThreads<NG>, 1)
     fd_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                      const __grid_constant__ CUtensorMap tmap_o, const PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_o,
+                      const PrefillParams p) {
   using Lay = PLayout<D>;
   constexpr int kD = D;
   constexpr int kNB = Lay::kNB;
@@ -352,8 +353,10 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
   uint64_t* q_ready = bars + 22;   // an item's q tiles are in shared memory
   uint64_t* drain = bars + 23;
   uint64_t* o_done = bars + 24;    // one head per CTA only: a P.V has completed
+  uint64_t* q_full = bars + 25;    // an item's q tiles (fp32) have landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 208);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 212);
+  uint64_t* q_free = bars + 27;    // the q areas may take the next item's q (one arrival per head)
 
   // Two query heads of one GQA group share an item (and every K/V tile) when
   // the group size is even: head G has S buffer G (TMEM columns 256 G) and O
@@ -378,12 +381,15 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
     mbar_init(q_ready, 4 * ngroups);
     mbar_init(drain, 1);
     mbar_init(o_done, 1);
+    mbar_init(q_full, 1);
+    mbar_init(q_free, ngroups);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
+    prefetch_tensormap(&tmap_q);
     prefetch_tensormap(&tmap_o);
   }
   if (warp == 1) {
@@ -403,10 +409,29 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     regs_dec<NG, kRegsLow>();
-    uint32_t u = 0;  // slot uses so far
-    Ring pr;         // the next use's slot
+    uint32_t u = 0;   // slot uses so far
+    uint32_t fq = 0;  // items with key tiles whose q this warp has loaded
+    Ring pr;          // the next use's slot
     for (int32_t idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
       const Item it = item_of(p, idx, ngroups, n_m);
+      if (it.n_tiles > 0) {
+        // the item's q tiles, fp32, into the heads' q areas (the softmax groups
+        // convert them there), once the previous item is done with those areas
+        if (lane == 0) {
+          if (fq > 0 && !bar_ok(q_free, (fq - 1) & 1u, abort_flag)) ok = false;
+          if (ok) {
+            mbar_arrive_expect_tx(q_full, (uint32_t)(ngroups * kD * kM * 4));
+#pragma unroll
+            for (int G = 0; G < ngroups; ++G)
+#pragma unroll
+              for (int blk = 0; blk < kD / 32; ++blk)
+                tma_load_3d(smem + (uint32_t)G * kQGroupBytes + (uint32_t)blk * kBlockBytes, &tmap_q, q_full, blk * 32,
+                            it.m0, it.b * p.Hq + it.h0 + G);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) ++fq;
+      }
       for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
         // lane l brings rows [16 l, 16 l + 16) of the tile: one page run when paged
         const int32_t t0 = j * kN;
@@ -446,6 +471,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
       const uint32_t first = u > nslots ? u - nslots : 0;
       for (uint32_t t = first; t < u; ++t)
         if (!mbar_wait(kv_full + t % nslots, (t / nslots) & 1)) atomicOr(p.err, kErrTimeout);
+      if (fq > 0 && !mbar_wait(q_full, (fq - 1) & 1u)) atomicOr(p.err, kErrTimeout);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -601,36 +627,57 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
       const int32_t qi = it.m0 + r;
       const int32_t lim = row_keys(p, it.L, qi);
       if (n > 0) {
-        // q rows, times scale*log2(e), as bf16 hi / lo in the swizzled A layout.  The
-        // previous item's S MMAs are all complete (this group saw its last S).  The
-        // warp loads its 32 rows together: each load instruction covers 512
-        // contiguous bytes (128 / D rows), 16 instructions in flight per batch.
-        {
-          constexpr int kLoads = 32 * kD / 128;  // per lane, for the warp's 32 rows
-          constexpr int kBatch = kLoads < 16 ? kLoads : 16;
-          const size_t head_row0 = ((size_t)it.b * p.Hq + h) * p.n_q;
-#pragma unroll 1
-          for (int i0 = 0; i0 < kLoads; i0 += kBatch) {
-            float4 v[kBatch];
+        // The item's q rows (fp32, landed by the producer's tensor loads in
+        // this head's q area as [D/32 blocks][128 rows][128 B], 128-byte
+        // swizzle), times scale*log2(e), become bf16 hi / lo in the swizzled A
+        // layout over the same bytes.  Row r of either layout fills row slot r
+        // of each 16 KB block, so every thread converts its own row in place:
+        // fp32 columns [32b, 32b+32) sit in block b, the hi of columns
+        // [64h, 64h+64) in block h and their lo in block D/64 + h; a block is
+        // read before it is written.  The previous item is done with this area
+        // (the producer waited for q_free before the loads).
+        if (ok && !bar_ok(q_full, f & 1, abort_flag)) ok = false;
+        auto load32 = [&](int blk, float* v) {
 #pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-              const int e = (i0 + i) * 128 + lane * 4;  // float index within the warp's rows
-              const int32_t row = quarter * 32 + e / kD, qr = it.m0 + row;
-              v[i] = qr < p.n_q ? __ldg(reinterpret_cast<const float4*>(p.q + (head_row0 + qr) * kD + e % kD))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-              const int e = (i0 + i) * 128 + lane * 4;
-              const uint32_t row = (uint32_t)(quarter * 32 + e / kD), col = (uint32_t)(e % kD);
-              uint32_t hi0, lo0, hi1, lo1;
-              split2(v[i].x * p.qk_scale, v[i].y * p.qk_scale, hi0, lo0);
-              split2(v[i].z * p.qk_scale, v[i].w * p.qk_scale, hi1, lo1);
-              const uint32_t off = (col >> 6) * 16384u + swz(row, (col >> 3) & 7u) + ((col >> 2) & 1u) * 8u;
-              sts64(qbase + kQhi + off, hi0, hi1);
-              sts64(qbase + kQlo + off, lo0, lo1);
-            }
+          for (int c = 0; c < 8; ++c) {
+            const float4 x = lds128(qbase + (uint32_t)blk * kBlockBytes + swz((uint32_t)r, (uint32_t)c));
+            v[4 * c] = x.x;
+            v[4 * c + 1] = x.y;
+            v[4 * c + 2] = x.z;
+            v[4 * c + 3] = x.w;
           }
+        };
+        // columns [64h, 64h+64) from v[64] -> hi block h, lo block kNB + h
+        auto store64 = [&](int hb, const float* v) {
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            uint32_t hi0, lo0, hi1, lo1;
+            split2(v[c] * p.qk_scale, v[c + 1] * p.qk_scale, hi0, lo0);
+            split2(v[c + 2] * p.qk_scale, v[c + 3] * p.qk_scale, hi1, lo1);
+            const uint32_t off = (uint32_t)hb * 16384u + swz((uint32_t)r, (uint32_t)(c >> 3)) + (uint32_t)((c >> 2) & 1) * 8u;
+            sts64(qbase + kQhi + off, hi0, hi1);
+            sts64(qbase + kQlo + off, lo0, lo1);
+          }
+        };
+        if constexpr (kD == 128) {
+          float v[96];
+          load32(0, v);
+          load32(1, v + 32);
+          load32(2, v + 64);
+          store64(0, v);  // hi -> block 0, lo -> block 2: both read
+          load32(3, v);
+          float w[64];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            w[i] = v[64 + i];
+            w[32 + i] = v[i];
+          }
+          store64(1, w);  // hi -> block 1, lo -> block 3: both read
+        } else {
+          float v[64];
+          load32(0, v);
+          load32(1, v + 32);
+          store64(0, v);  // hi -> block 0, lo -> block 1
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -732,7 +779,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         tc_fence_after();
       }
       const float inv = l > 0.f && ok ? 1.f / l : 0.f;
-      if constexpr (NG == 2) {
+      if (NG == 2 && n > 0) {
         // O / l goes through this head's q area, free now (every S MMA of the
         // item has completed before its last P.V): [D/32 blocks][128 rows][128 B]
         // with the 128-byte swizzle, then out with tensor stores of 32 columns x
@@ -741,12 +788,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
 #pragma unroll 1
         for (int c4 = 0; c4 < kD / 32; ++c4) {
           float o[32];
-          if (n > 0) {
-            tmem_ld32(obase + (uint32_t)c4 * 32, o);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0.f;
-          }
+          tmem_ld32(obase + (uint32_t)c4 * 32, o);
           const uint32_t blk = qbase + (uint32_t)c4 * kBlockBytes;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
@@ -754,7 +796,18 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
                    __float_as_uint(o[4 * c + 1] * inv), __float_as_uint(o[4 * c + 2] * inv),
                    __float_as_uint(o[4 * c + 3] * inv));
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the staged rows, for the tensor stores
+        named_barrier(1 + G, 128);
+        if (warp == kSoftmax0<NG> + 4 * G && lane == 0) {
+#pragma unroll
+          for (int c4 = 0; c4 < kD / 32; ++c4)
+            tma_store_3d(&tmap_o, qbase + (uint32_t)c4 * kBlockBytes, c4 * 32, it.m0, it.b * p.Hq + h);
+          bulk_commit_group();
+          bulk_wait_read_all();  // the q area is free again (and the CTA may exit)
+          mbar_arrive(q_free);
+        }
       } else {
+        // one head per CTA (short CTAs), or an item without keys: direct stores
         float* orow = p.out + (((size_t)it.b * p.Hq + h) * p.n_q + qi) * kD;
 #pragma unroll 1
         for (int c4 = 0; c4 < kD / 32; ++c4) {
@@ -772,21 +825,11 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
                   make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
           }
         }
+        // every S MMA of the item has completed (o_final): the q area may take the next q
+        if (n > 0 && warp == kSoftmax0<NG> + 4 * G && lane == 0) mbar_arrive(q_free);
       }
       if (qi < p.n_q && p.lse)
         p.lse[((size_t)it.b * p.Hq + h) * p.n_q + qi] = l > 0.f ? (mref + log2f(l)) * kLn2f : -INFINITY;
-      if constexpr (NG == 2) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the staged rows, for the tensor stores
-        named_barrier(1 + G, 128);
-        if (warp == kSoftmax0<NG> + 4 * G && lane == 0) {
-#pragma unroll
-          for (int c4 = 0; c4 < kD / 32; ++c4)
-            tma_store_3d(&tmap_o, qbase + (uint32_t)c4 * kBlockBytes, c4 * 32, it.m0, it.b * p.Hq + h);
-          bulk_commit_group();
-          bulk_wait_read_all();  // the q area is free for the next item's q (and the CTA may exit)
-        }
-        named_barrier(1 + G, 128);
-      }
       // this group's O columns are read before the next item's first P.V (which
       // needs this group's P) overwrites them
       tc_fence_before();
@@ -807,8 +850,8 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
 }
 
 template <int D, int NG>
-cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-                             const PrefillParams& p, cudaStream_t stream) {
+cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                             const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream) {
   static int configured = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -830,19 +873,21 @@ cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const
   const int64_t items = (int64_t)((p.n_q + kM - 1) / kM) * (p.Hq / NG) * p.B;
   if (items > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)items);
-  fd_prefill_kernel<D, NG><<<grid, kThreads<NG>, PLayout<D>::kSmemAlloc, stream>>>(tk, tv, to, p);
+  fd_prefill_kernel<D, NG><<<grid, kThreads<NG>, PLayout<D>::kSmemAlloc, stream>>>(tk, tv, tq, to, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(int D, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-                           const PrefillParams& p, cudaStream_t stream) {
+cudaError_t launch_prefill(int D, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                           const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream) {
   const bool pair = p.g % 2 == 0;  // two query heads per CTA
   if (D == 128)
-    return pair ? launch_prefill_t<128, 2>(tk, tv, to, p, stream) : launch_prefill_t<128, 1>(tk, tv, to, p, stream);
+    return pair ? launch_prefill_t<128, 2>(tk, tv, tq, to, p, stream)
+                : launch_prefill_t<128, 1>(tk, tv, tq, to, p, stream);
   if (D == 64)
-    return pair ? launch_prefill_t<64, 2>(tk, tv, to, p, stream) : launch_prefill_t<64, 1>(tk, tv, to, p, stream);
+    return pair ? launch_prefill_t<64, 2>(tk, tv, tq, to, p, stream)
+                : launch_prefill_t<64, 1>(tk, tv, tq, to, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -25,9 +25,10 @@ constexpr int kPrefillRows = 128;
 constexpr int kPrefillKeys = 128;
 
 // D = 64 or 128; cudaErrorInvalidValue otherwise.
-// `to`: the output [B*Hq, n_q, D] fp32, 32-column x 128-row boxes with the
-// 128-byte swizzle (the kernel's epilogue stores through it).
-cudaError_t launch_prefill(int D, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-                           const PrefillParams& p, cudaStream_t stream);
+// `tq`, `to`: q and the output as [B*Hq, n_q, D] fp32, 32-column x 128-row
+// boxes with the 128-byte swizzle (the kernel loads q tiles and stores output
+// tiles through them).
+cudaError_t launch_prefill(int D, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                           const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream);
 
 }  // namespace fdk
