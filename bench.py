@@ -78,6 +78,17 @@ def source_hash(sources=KERNEL_SOURCES) -> str:
     return h.hexdigest()[:12]
 
 
+def prefill_l2_note(N: int, hkv: int) -> str:
+    """What one prefill step touches (q, K/V, output) against the L2 size: each step re-reads q and K/V."""
+    q = 32 * N * 128 * 4
+    kv = 2 * hkv * N * 128 * 2
+    total = 2 * q + kv
+    if total > L2_BYTES:
+        return (f"q {q / 1e6:.0f} MB + K/V {kv / 1e6:.0f} MB + output {q / 1e6:.0f} MB = {total / 1e6:.0f} MB per step "
+                f"> {L2_BYTES / 1e6:.0f} MB L2; no flush")
+    return f"q, K/V and output {total / 1e6:.1f} MB per step fit in L2 (warm: no flush)"
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -707,7 +718,7 @@ def run_prefill(args):
         "data": "synthetic",
         "config": {"workload": spec.name, "B": 1, "Hq": 32, "Hkv": hkv, "D": 128, "n_q": N, "keys": N,
                    "causal": True, "kv_dtype": "bf16", "q_dtype": "f32", "flops_per_step": flops,
-                   "launch": "one CUDA graph of K fd_prefill calls",
+                   "launch": "one CUDA graph of K fd_prefill calls", "l2": prefill_l2_note(N, hkv),
                    "kernel": "fd_prefill_kernel (tcgen05.mma M=128; q and p as bf16 hi+lo: 2 MMAs per product)"},
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
                      "traffic": recorded_traffic(spec.name, PREFILL_SOURCES), "peak_source": peak_src,
