@@ -200,3 +200,20 @@ def test_prefill_writes_only_its_rows(hq, hkv, d):
     ref_out, ref_lse = oracle_rows(case, q, True)
     assert_close(np64(out), ref_out, "out")
     assert_close(np64(lse), ref_lse, "lse")
+
+
+@pytest.mark.parametrize("hq,hkv,B,n_q", [(32, 8, 2, 1280), (6, 2, 8, 512)],
+                         ids=["two_heads_per_cta", "one_head_per_cta"])
+def test_prefill_more_items_than_sms(hq, hkv, B, n_q):
+    """More 128-row query tiles than SMs, so that CTAs run in waves and each SM
+    takes several items in turn, with sequences without keys among them: every
+    output matches the oracle."""
+    spec = small_spec("many_items", B, hq, hkv, 128, 1400, seed=33)
+    lengths = [0, 800, 650, 700, 720, 0, 790, 800] if B > 2 else [1400, 0]
+    case = make_case(spec, "cuda", lengths=lengths)
+    q = window_q(case, n_q, seed=14)
+    out, lse = run_prefill(case, q, True)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle_rows(case, q, True)
+    assert_close(np64(out), ref_out, "out")
+    assert_close(np64(lse), ref_lse, "lse")
