@@ -738,17 +738,20 @@ __device__ __forceinline__ void merge_pair_smem(const SplitParams& p, uint8_t* s
   }
   named_barrier(1, kCons);
   // Item (h, j): head h, output elements [j*EPL, (j+1)*EPL).  Thread tid takes
-  // items tid + i*kCons, i < IPT (one head per warp and i), all at once.
+  // items tid + i*kCons, i < IPT (one head per warp and i), all at once.  The
+  // split loop has no branch, so the loads of all items and splits of a step
+  // are in flight together: splits past `count` (up to the next multiple of 4)
+  // read a valid state with weight 0 (sw is 0 there), and fmaf(0, v, a) == a
+  // for finite v, so the sums keep merge_head's bits.  Items of heads past nh
+  // read head 0 and are not stored.
   float acc[IPT][4][EPL];
   uint32_t wa[IPT], oa[IPT];  // shared addresses: the item's weights and its slice of split 0
-  bool live[IPT];
   const uint32_t kstep = (uint32_t)stride * D * 4;  // bytes from split k to k + 1
 #pragma unroll
   for (int i = 0; i < IPT; ++i) {
     const int item = tid + i * kCons;
     const int h = item >> 5, j = item & 31;
     const int hc = h < nh ? h : 0;
-    live[i] = item < nh * 32 && shead[2 * hc] != -INFINITY;
     wa[i] = smem_addr(sw + hc * 128);
     oa[i] = smem_addr(so) + (uint32_t)((hc * hs * D + j * EPL) * 4);
 #pragma unroll
@@ -756,31 +759,29 @@ __device__ __forceinline__ void merge_pair_smem(const SplitParams& p, uint8_t* s
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc[i][s4][e] = 0.f;
   }
+  const int klast = count - 1;
   for (int k0 = 0; k0 < count; k0 += 4) {
 #pragma unroll
     for (int i = 0; i < IPT; ++i) {
-      if (!live[i]) continue;
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         const int k = k0 + jj;
-        if (k < count) {
-          const float w = __uint_as_float(lds32u(wa[i] + 4 * k));
-          const uint32_t va = oa[i] + (uint32_t)k * kstep;
-          float vv[EPL];
-          if constexpr (EPL == 4) {
-            const float4 x = lds128(va);
-            vv[0] = x.x;
-            vv[1] = x.y;
-            vv[2] = x.z;
-            vv[3] = x.w;
-          } else {
-            const uint2 x = lds64u(va);
-            vv[0] = __uint_as_float(x.x);
-            vv[1] = __uint_as_float(x.y);
-          }
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[i][jj][e] = fmaf(w, vv[e], acc[i][jj][e]);
+        const float w = __uint_as_float(lds32u(wa[i] + 4 * k));
+        const uint32_t va = oa[i] + (uint32_t)(k < klast ? k : klast) * kstep;
+        float vv[EPL];
+        if constexpr (EPL == 4) {
+          const float4 x = lds128(va);
+          vv[0] = x.x;
+          vv[1] = x.y;
+          vv[2] = x.z;
+          vv[3] = x.w;
+        } else {
+          const uint2 x = lds64u(va);
+          vv[0] = __uint_as_float(x.x);
+          vv[1] = __uint_as_float(x.y);
         }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[i][jj][e] = fmaf(w, vv[e], acc[i][jj][e]);
       }
     }
   }
@@ -791,15 +792,15 @@ __device__ __forceinline__ void merge_pair_smem(const SplitParams& p, uint8_t* s
     const int h = item >> 5, j = item & 31;
     float* orow = out_rows + (size_t)h * D + j * EPL;
     const float mx = shead[2 * h], L = shead[2 * h + 1];
-    if (mx == -INFINITY) {
+    float o4[EPL];
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) orow[e] = 0.f;
-      if (lse_slots && j == 0) lse_slots[h] = -INFINITY;
-      continue;
-    }
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) orow[e] = (((acc[i][0][e] + acc[i][1][e]) + acc[i][2][e]) + acc[i][3][e]) / L;
-    if (lse_slots && j == 0) lse_slots[h] = mx + logf(L);
+    for (int e = 0; e < EPL; ++e)
+      o4[e] = mx == -INFINITY ? 0.f : (((acc[i][0][e] + acc[i][1][e]) + acc[i][2][e]) + acc[i][3][e]) / L;
+    if constexpr (EPL == 4)
+      *reinterpret_cast<float4*>(orow) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+    else
+      *reinterpret_cast<float2*>(orow) = make_float2(o4[0], o4[1]);
+    if (lse_slots && j == 0) lse_slots[h] = mx == -INFINITY ? -INFINITY : mx + logf(L);
   }
 }
 
