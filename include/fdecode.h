@@ -211,7 +211,9 @@ FD_API fd_status fd_append_decode(const float* q, const void* k_new, const void*
  * FlashAttention's tiling along them; decode has one.
  *   Supports D = 64 and 128 with a bf16 cache (contiguous or paged); any n_q >= 1.
  *   workspace: at least 256 bytes, zero-filled once (its first word is the
- *   kernels' error word, read by fd_workspace_status).  out, lse as in
+ *   kernels' error word, read by fd_workspace_status; bytes 128-135 hold the
+ *   kernel's work-queue counters, which every call leaves at zero, so calls
+ *   that share a workspace must not overlap in time).  out, lse as in
  *   fd_decode_rows.  One launch, asynchronous on `stream`.
  *   FD_ERR_CUDA, with nothing launched, also when the kernel variant for an odd
  *   group size (one query head per CTA, which redistributes registers between

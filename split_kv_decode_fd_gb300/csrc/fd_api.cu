@@ -20,6 +20,7 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr size_t kHeaderBytes = 256;  // error word + reserved
+constexpr size_t kPrefillWorkOff = 128;  // the prefill's item-queue counters, inside the header
 // Arrival counters of the fused merge live in a region of fixed size right
 // after the header, whatever the problem shape, so that no call ever writes
 // partials where another shape keeps its counters; every call leaves the
@@ -490,6 +491,7 @@ fd_status fd_prefill(const float* q, int32_t n_q, int32_t causal, const fd_kv_de
   p.seq_lens = seq_lens;
   p.block_table = kv->block_table;
   p.err = reinterpret_cast<unsigned*>(workspace);
+  p.work = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + kPrefillWorkOff);
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;

@@ -15,6 +15,7 @@ struct PrefillParams {
   const int32_t* seq_lens;     // [B] keys per sequence (the n_q rows are its last n_q tokens), or null
   const int32_t* block_table;  // paged: [B, max_pages]
   unsigned* err;               // error word (timeouts, bad pages)
+  unsigned* work;              // [2] item queue: next item, CTAs done (zero between launches)
   int32_t B, Hq, Hkv, g, n_q, max_len, causal;
   int32_t paged, page_size, max_pages, num_pages;
   float qk_scale;              // scale * log2(e)
