@@ -217,3 +217,23 @@ def test_prefill_more_items_than_sms(hq, hkv, B, n_q):
     ref_out, ref_lse = oracle_rows(case, q, True)
     assert_close(np64(out), ref_out, "out")
     assert_close(np64(lse), ref_lse, "lse")
+
+
+def test_prefill_queue_counters_return_to_zero():
+    """With two heads per CTA and more query tiles than SMs, CTAs take items from
+    two counters in the workspace header (bytes 128-135): the last CTA leaves
+    both at zero, and the results do not depend on which CTA took which item."""
+    spec = small_spec("queue", 2, 32, 8, 128, 1300, seed=35)
+    case = make_case(spec, "cuda", lengths=[1300, 1290])
+    q = window_q(case, 1280, seed=15)
+    ws = fd.Workspace()
+    first = run_prefill(case, q, True, workspace=ws)
+    torch.cuda.synchronize()
+    hdr = ws.buf[128:136].cpu()
+    assert torch.all(hdr == 0), f"queue counters left at {hdr.tolist()}"
+    for _ in range(3):
+        again = run_prefill(case, q, True, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(again[0], first[0]) and torch.equal(again[1], first[1])
+    assert torch.all(ws.buf[128:136].cpu() == 0)
+    assert fd.workspace_status(ws) == 0
