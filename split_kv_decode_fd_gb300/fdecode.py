@@ -193,7 +193,13 @@ def _kv_desc(k, v, block_table):
 
 
 class Workspace:
-    """Zero-initialised device scratch for fd_decode, grown on demand."""
+    """Zero-initialised device scratch for the kernels, grown on demand.
+
+    It holds the error word, the decode kernels' arrival counters and partial
+    states, and the prefill's item queue, all left at zero between calls: calls
+    that may run at the same time (on different streams) need a Workspace each.
+    The default one, used when none is passed, is shared per device.
+    """
 
     def __init__(self, device=None):
         self.device = device
