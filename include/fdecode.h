@@ -344,13 +344,14 @@ FD_API int64_t fd_plan_pieces(int32_t B, int32_t Hq, int32_t Hkv, int32_t kv_dty
 
 /*
  * Testing hook for the kernels' bounded waits; off by default.  Every
- * mbarrier wait of the split kernel gives up after a time limit (2 s by
- * default), records FD_ERR_TIMEOUT in the error word, lets the copies it
- * issued land and exits, so the context stays usable.  With stage >= 0, the
- * split kernels launched afterwards (fd_decode and every call built on it,
- * fd_split_partial) skip the copies of stage number `stage` in every CTA that
- * reaches it, so the waits for that stage run out; wait_limit_ns > 0 shortens every
- * wait of those kernels to that many nanoseconds (0 keeps the default).  The
+ * mbarrier wait of the split and prefill kernels gives up after a time limit
+ * (2 s by default), records FD_ERR_TIMEOUT in the error word, lets the copies
+ * it issued land and exits, so the context stays usable.  With stage >= 0, the
+ * kernels launched afterwards skip, in every CTA that reaches it, the copies of
+ * stage number `stage` (split kernels: fd_decode and every call built on it,
+ * fd_split_partial) or K/V tile copy number `stage` (fd_prefill, K and V
+ * counted separately), so the waits for it run out; wait_limit_ns > 0 shortens
+ * every wait of those kernels to that many nanoseconds (0 keeps the default).  The
  * call's output is then undefined and fd_workspace_status (or
  * fd_static_status) reports FD_ERR_TIMEOUT; the workspace stays valid for the
  * next call.  stage < 0 switches the hook off and restores the default limit.

@@ -504,6 +504,8 @@ fd_status fd_prefill(const float* q, int32_t n_q, int32_t causal, const fd_kv_de
   p.max_pages = kv->max_pages_per_seq;
   p.num_pages = kv->num_pages;
   p.qk_scale = (float)((double)scale * 1.4426950408889634);
+  p.stall_u = g_stall_it.load(std::memory_order_relaxed);
+  p.wait_ns = (uint64_t)g_wait_ns.load(std::memory_order_relaxed);
   return launch_prefill(D, tk, tv, tq, to, p, (cudaStream_t)stream) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 

@@ -272,13 +272,16 @@ __device__ __forceinline__ int32_t row_keys(const PrefillParams& p, int32_t L, i
 // Waits of every role: false when the CTA aborts or the wait times out.  A
 // phase that has already completed costs one try_wait; the abort flag is read
 // only when the thread has to wait.
-__device__ __forceinline__ bool bar_ok(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  return mbar_try_wait(bar, parity) || (!*abort_flag && mbar_wait(bar, parity));
+// limit_ns: the kernel's wait limit, used only when the phase is not complete
+// at the first try.
+__device__ __forceinline__ bool bar_ok(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                       unsigned long long limit_ns) {
+  return mbar_try_wait(bar, parity) || (!*abort_flag && mbar_wait_for(bar, parity, limit_ns));
 }
 
-// The MMA thread's waits, followed by the tcgen05 fence its MMAs need.
-__device__ __forceinline__ bool wait_ok(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  const bool r = bar_ok(bar, parity, abort_flag);
+__device__ __forceinline__ bool wait_ok(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                        unsigned long long limit_ns) {
+  const bool r = bar_ok(bar, parity, abort_flag, limit_ns);
   tc_fence_after();
   return r;
 }
@@ -331,7 +334,7 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int32_t idx, int
 // far, and f, the items with at least one tile so far.  Slot uses are numbered
 // u = 2 g (K) and 2 g + 1 (V): slot u % nslots, phase u / nslots.
 // NG: query heads per CTA, 2 when the GQA group size is even, else 1.
-template <int D, int NG>
+template <int D, int NG, bool kHook>
 __global__ void __launch_bounds__(kThreads<NG>, 1)
     fd_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                       const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_o,
@@ -418,6 +421,9 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
   cta_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Every wait's limit: the default, or with the testing hook the call's
+  // (the instance without the hook keeps the constant).
+  const unsigned long long wl = kHook && p.wait_ns ? p.wait_ns : kWaitLimitNs;
   bool ok = true;
 
   // Each role sets its register count first thing, so that the compiler
@@ -427,6 +433,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
     regs_dec<NG, kRegsLow>();
     uint32_t u = 0;   // slot uses so far
     uint32_t fq = 0;  // items with key tiles whose q this warp has loaded
+    uint32_t stalled = 0xffffffffu;  // the copy skipped by the testing hook
     Ring pr;          // the next use's slot
     for (uint32_t e = 0;; ++e) {
       // take the next item (longest first) and announce it; -1 ends the walk
@@ -434,7 +441,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
       if constexpr (NG == 2) {
         if (lane == 0) {
           const uint32_t sl = e & 1u;
-          if (e >= 2 && ok && !bar_ok(item_empty + sl, ((e >> 1) & 1u) ^ 1u, abort_flag)) ok = false;
+          if (e >= 2 && ok && !bar_ok(item_empty + sl, ((e >> 1) & 1u) ^ 1u, abort_flag, wl)) ok = false;
           if (ok) {
             // the first item is the CTA's own; then, with fewer CTAs than items,
             // the next one not yet taken
@@ -457,7 +464,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         // the item's q tiles, fp32, into the heads' q areas (the softmax groups
         // convert them there), once the previous item is done with those areas
         if (lane == 0) {
-          if (fq > 0 && !bar_ok(q_free, (fq - 1) & 1u, abort_flag)) ok = false;
+          if (fq > 0 && !bar_ok(q_free, (fq - 1) & 1u, abort_flag, wl)) ok = false;
           if (ok) {
             mbar_arrive_expect_tx(q_full, (uint32_t)(ngroups * kD * kM * 4));
 #pragma unroll
@@ -490,9 +497,15 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         const unsigned issue = __ballot_sync(0xffffffffu, mine);
         for (int kv = 0; kv < 2; ++kv, ++u, pr = pr.next(1, nslots)) {
           const uint32_t slot = pr.slot;
-          if (lane == 0 && !bar_ok(kv_empty + slot, pr.phase ^ 1u, abort_flag)) ok = false;
+          if (lane == 0 && !bar_ok(kv_empty + slot, pr.phase ^ 1u, abort_flag, wl)) ok = false;
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
+          if (kHook && p.stall_u >= 0 && u == (uint32_t)p.stall_u) {
+            // testing hook: nothing is issued for this copy, so the waits for it run
+            // out (and nothing is left in flight)
+            stalled = u;
+            continue;
+          }
           if (lane == 0) mbar_arrive_expect_tx(kv_full + slot, (uint32_t)__popc(issue) * kNB * 2048u);
           __syncwarp();
           if (mine) {
@@ -509,8 +522,8 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
     if (lane == 0) {
       const uint32_t first = u > nslots ? u - nslots : 0;
       for (uint32_t t = first; t < u; ++t)
-        if (!mbar_wait(kv_full + t % nslots, (t / nslots) & 1)) atomicOr(p.err, kErrTimeout);
-      if (fq > 0 && !mbar_wait(q_full, (fq - 1) & 1u)) atomicOr(p.err, kErrTimeout);
+        if (t != stalled && !mbar_wait_for(kv_full + t % nslots, (t / nslots) & 1, wl)) atomicOr(p.err, kErrTimeout);
+      if (fq > 0 && !mbar_wait_for(q_full, (fq - 1) & 1u, wl)) atomicOr(p.err, kErrTimeout);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -555,7 +568,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         int32_t idx;
         if constexpr (NG == 2) {
           const uint32_t sl = e & 1u;
-          if (!wait_ok(item_full + sl, (e >> 1) & 1u, abort_flag)) {
+          if (!wait_ok(item_full + sl, (e >> 1) & 1u, abort_flag, wl)) {
             ok = false;
             break;
           }
@@ -569,7 +582,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         const Item it = item_of(p, idx, ngroups, n_m);
         const int32_t n = it.n_tiles;
         if (n == 0) continue;  // no q_ready phase either: the softmax skips such items too
-        if (!wait_ok(q_ready, f & 1, abort_flag)) {
+        if (!wait_ok(q_ready, f & 1, abort_flag, wl)) {
           ok = false;
           break;
         }
@@ -578,7 +591,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
           for (int32_t j = 0; j < n; ++j) {
             const uint32_t gj = g + (uint32_t)j;
             const Ring vr = kr.next(1, nslots);  // V of this tile
-            if (!wait_ok(kv_full + kr.slot, kr.phase, abort_flag)) {
+            if (!wait_ok(kv_full + kr.slot, kr.phase, abort_flag, wl)) {
               ok = false;
               break;
             }
@@ -586,7 +599,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
             umma_commit(s_full + 0);
             if (j >= 1) {
               // head 1's P.V of the previous tile, then its S of this tile
-              if (!wait_ok(p_full + 1, (gj - 1) & 1, abort_flag)) {
+              if (!wait_ok(p_full + 1, (gj - 1) & 1, abort_flag, wl)) {
                 ok = false;
                 break;
               }
@@ -596,7 +609,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
             issue_s(256, 1, kr.slot);
             umma_commit(s_full + 1);
             umma_commit(kv_empty + kr.slot);
-            if (!wait_ok(kv_full + vr.slot, vr.phase, abort_flag) || !wait_ok(p_full + 0, gj & 1, abort_flag)) {
+            if (!wait_ok(kv_full + vr.slot, vr.phase, abort_flag, wl) || !wait_ok(p_full + 0, gj & 1, abort_flag, wl)) {
               ok = false;
               break;
             }
@@ -606,7 +619,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
             kr = kr.next(2, nslots);
           }
           if (!ok) break;
-          if (!wait_ok(p_full + 1, (g + (uint32_t)n - 1) & 1, abort_flag)) {
+          if (!wait_ok(p_full + 1, (g + (uint32_t)n - 1) & 1, abort_flag, wl)) {
             ok = false;
             break;
           }
@@ -620,7 +633,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
             const Ring vcur = kr.next(1, nslots);
             if (j < n) {
               const uint32_t gj = g + (uint32_t)j;
-              if (!wait_ok(kv_full + kr.slot, kr.phase, abort_flag)) {
+              if (!wait_ok(kv_full + kr.slot, kr.phase, abort_flag, wl)) {
                 ok = false;
                 break;
               }
@@ -630,8 +643,8 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
             }
             if (j >= 1) {
               const uint32_t gp = g + (uint32_t)j - 1;
-              if (!wait_ok(kv_full + vprev.slot, vprev.phase, abort_flag) ||
-                  !wait_ok(p_full + (gp & 1), (gp >> 1) & 1, abort_flag)) {
+              if (!wait_ok(kv_full + vprev.slot, vprev.phase, abort_flag, wl) ||
+                  !wait_ok(p_full + (gp & 1), (gp >> 1) & 1, abort_flag, wl)) {
                 ok = false;
                 break;
               }
@@ -656,7 +669,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
       }
       // every MMA this thread issued has finished before TMEM is released
       umma_commit(drain);
-      if (!mbar_wait(drain, 0)) atomicOr(p.err, kErrTimeout);
+      if (!mbar_wait_for(drain, 0, wl)) atomicOr(p.err, kErrTimeout);
     }
   } else if (warp < kSoftmax0<NG>) {
     regs_dec<NG, kRegsLow>();  // no role
@@ -678,7 +691,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
       if constexpr (NG == 2) {
         if (lane == 0) {
           const uint32_t sl = e & 1u;
-          if (bar_ok(item_full + sl, (e >> 1) & 1u, abort_flag)) idx = item_slot[sl];
+          if (bar_ok(item_full + sl, (e >> 1) & 1u, abort_flag, wl)) idx = item_slot[sl];
           mbar_arrive(item_empty + sl);
         }
         idx = __shfl_sync(0xffffffffu, idx, 0);
@@ -702,7 +715,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         // [64h, 64h+64) in block h and their lo in block D/64 + h; a block is
         // read before it is written.  The previous item is done with this area
         // (the producer waited for q_free before the loads).
-        if (ok && !bar_ok(q_full, f & 1, abort_flag)) ok = false;
+        if (ok && !bar_ok(q_full, f & 1, abort_flag, wl)) ok = false;
         auto load32 = [&](int blk, float* v) {
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -757,7 +770,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         const uint32_t gj = g + (uint32_t)j;
         const uint32_t buf = dual ? (gj & 1) : (uint32_t)G, par = dual ? (gj >> 1) & 1 : gj & 1;
         const uint32_t tbase = tmem + buf * 256u + lane_off;  // this tile's S / P
-        if (ok && !bar_ok(s_full + buf, par, abort_flag)) ok = false;
+        if (ok && !bar_ok(s_full + buf, par, abort_flag, wl)) ok = false;
         tc_fence_after();
         float s[kN];
 #pragma unroll
@@ -807,7 +820,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         // (.sync.aligned): the whole warp rescales when any of its rows must,
         // the others with alpha = 1.
         if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
-          if (dual && ok && !bar_ok(o_done, (gj - 1) & 1, abort_flag)) ok = false;
+          if (dual && ok && !bar_ok(o_done, (gj - 1) & 1, abort_flag, wl)) ok = false;
           tc_fence_after();
 #pragma unroll 1
           for (int c4 = 0; c4 < kD / 32; ++c4) {
@@ -822,7 +835,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
           // keys past L in the last tile get p = 0, but 0 * NaN is NaN: zero those V
           // rows (head 0 does it for both: its P.V is issued first)
           const uint32_t uv = 2 * gj + 1, slot = uv % nslots;
-          if (ok && !bar_ok(kv_full + slot, (uv / nslots) & 1, abort_flag)) ok = false;
+          if (ok && !bar_ok(kv_full + slot, (uv / nslots) & 1, abort_flag, wl)) ok = false;
           const int32_t nvalid = it.L - j * kN;
           const uint32_t vt = sbase + Lay::slot_off(slot);
           const int32_t tid2 = (warp - kSoftmax0<NG>) * 32 + lane;
@@ -841,7 +854,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
       // ---- epilogue: out = O / l, lse = ln(sum of exp).  n is the same for the
       // whole CTA, so the collective loads run on every lane or none.
       if (n > 0) {
-        if (ok && !bar_ok(o_final + G, f & 1, abort_flag)) ok = false;
+        if (ok && !bar_ok(o_final + G, f & 1, abort_flag, wl)) ok = false;
         tc_fence_after();
       }
       const float inv = l > 0.f && ok ? 1.f / l : 0.f;
@@ -924,7 +937,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
   }
 }
 
-template <int D, int NG>
+template <int D, int NG, bool kHook>
 cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                              const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream) {
   static int configured = -1;
@@ -934,10 +947,10 @@ cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const
   if (configured != dev) {
     // the setmaxnreg split assumes this launch register count: refuse any other
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, fd_prefill_kernel<D, NG>);
+    e = cudaFuncGetAttributes(&fa, fd_prefill_kernel<D, NG, kHook>);
     if (e != cudaSuccess) return e;
     if (NG == 1 && fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(fd_prefill_kernel<D, NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fd_prefill_kernel<D, NG, kHook>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)PLayout<D>::kSmemAlloc);
     if (e != cudaSuccess) return e;
     configured = dev;
@@ -959,7 +972,7 @@ cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const
   // per CTA: a CTA per item, handed out by the hardware in index order (the
   // queue measured +1.6 % / +3.6 % there).
   const dim3 grid((unsigned)(NG == 2 && items > sms ? sms : items));
-  fd_prefill_kernel<D, NG><<<grid, kThreads<NG>, PLayout<D>::kSmemAlloc, stream>>>(tk, tv, tq, to, p);
+  fd_prefill_kernel<D, NG, kHook><<<grid, kThreads<NG>, PLayout<D>::kSmemAlloc, stream>>>(tk, tv, tq, to, p);
   return cudaGetLastError();
 }
 
@@ -968,12 +981,23 @@ cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const
 cudaError_t launch_prefill(int D, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                            const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream) {
   const bool pair = p.g % 2 == 0;  // two query heads per CTA
-  if (D == 128)
-    return pair ? launch_prefill_t<128, 2>(tk, tv, tq, to, p, stream)
-                : launch_prefill_t<128, 1>(tk, tv, tq, to, p, stream);
-  if (D == 64)
-    return pair ? launch_prefill_t<64, 2>(tk, tv, tq, to, p, stream)
-                : launch_prefill_t<64, 1>(tk, tv, tq, to, p, stream);
+  // the testing hook (fd_debug_stall) runs in instances of their own, so that
+  // the ordinary ones keep constant wait limits and no skip test
+  const bool hook = p.stall_u >= 0 || p.wait_ns != 0;
+  if (D == 128) {
+    if (hook)
+      return pair ? launch_prefill_t<128, 2, true>(tk, tv, tq, to, p, stream)
+                  : launch_prefill_t<128, 1, true>(tk, tv, tq, to, p, stream);
+    return pair ? launch_prefill_t<128, 2, false>(tk, tv, tq, to, p, stream)
+                : launch_prefill_t<128, 1, false>(tk, tv, tq, to, p, stream);
+  }
+  if (D == 64) {
+    if (hook)
+      return pair ? launch_prefill_t<64, 2, true>(tk, tv, tq, to, p, stream)
+                  : launch_prefill_t<64, 1, true>(tk, tv, tq, to, p, stream);
+    return pair ? launch_prefill_t<64, 2, false>(tk, tv, tq, to, p, stream)
+                : launch_prefill_t<64, 1, false>(tk, tv, tq, to, p, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

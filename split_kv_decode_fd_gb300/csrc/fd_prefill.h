@@ -19,6 +19,8 @@ struct PrefillParams {
   int32_t B, Hq, Hkv, g, n_q, max_len, causal;
   int32_t paged, page_size, max_pages, num_pages;
   float qk_scale;              // scale * log2(e)
+  uint64_t wait_ns;            // limit of every mbarrier wait (0: the default, 2 s)
+  int32_t stall_u;             // testing hook: the K/V copy (slot use) every CTA skips, or -1
 };
 
 // Query rows per CTA and keys per tile of the prefill kernel.
