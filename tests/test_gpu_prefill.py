@@ -202,13 +202,19 @@ def test_prefill_writes_only_its_rows(hq, hkv, d):
     assert_close(np64(lse), ref_lse, "lse")
 
 
-@pytest.mark.parametrize("hq,hkv,B,n_q", [(32, 8, 2, 1280), (6, 2, 8, 512)],
-                         ids=["two_heads_per_cta", "one_head_per_cta"])
-def test_prefill_more_items_than_sms(hq, hkv, B, n_q):
-    """More 128-row query tiles than SMs, so that CTAs run in waves and each SM
-    takes several items in turn, with sequences without keys among them: every
-    output matches the oracle."""
-    spec = small_spec("many_items", B, hq, hkv, 128, 1400, seed=33)
+@pytest.mark.parametrize("hq,hkv,B,n_q,d,layout,page", [(32, 8, 2, 1280, 128, "contiguous", 16),
+                                                       (6, 2, 8, 512, 128, "contiguous", 16),
+                                                       (32, 8, 2, 1280, 64, "contiguous", 16),
+                                                       (32, 8, 2, 1280, 128, "paged", 16),
+                                                       (32, 8, 2, 1280, 128, "paged", 64)],
+                         ids=["two_heads_per_cta", "one_head_per_cta", "two_heads_d64", "two_heads_paged16",
+                              "two_heads_paged64"])
+def test_prefill_more_items_than_sms(hq, hkv, B, n_q, d, layout, page):
+    """More 128-row query tiles than SMs: with two heads per CTA the CTAs take
+    items from the queue, with one head they run in waves; sequences without
+    keys among them, contiguous and paged caches: every output matches the
+    oracle."""
+    spec = small_spec("many_items", B, hq, hkv, d, 1400, layout=layout, page_size=page, seed=33)
     lengths = [0, 800, 650, 700, 720, 0, 790, 800] if B > 2 else [1400, 0]
     case = make_case(spec, "cuda", lengths=lengths)
     q = window_q(case, n_q, seed=14)
