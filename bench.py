@@ -553,7 +553,8 @@ def run_fdecode(args):
             torch.cuda.current_stream(device).synchronize()
     else:
         # a decode loop's view: the same pinned host buffers every step, arguments marshalled once
-        e2e_api = "fd_decode_host via HostDecoder" if not args.unfused else e2e_api
+        e2e_api = ("fd_decode_host via HostDecoder (pinned q, lengths, out, lse: read and written by the kernels "
+                   "over the host link every step)") if not args.unfused else e2e_api
         e2e_step = fd.HostDecoder(q_host, case.k, case.v, seq_lens_host=lens_host, max_seq_len=case.max_seq_len,
                                   block_table=case.block_table, scale=spec.scale, n_splits=spec.n_splits,
                                   out_host=out_h, lse_host=lse_h, workspace=ws_h)

@@ -271,12 +271,16 @@ FD_API fd_status fd_combine(const float* o_part, const float* m_part, const floa
                      float* lse, int32_t B, int32_t Hq, int32_t D, int32_t n_splits, void* stream);
 
 /*
- * fd_decode with the per-step inputs and outputs in HOST memory: copies
- * q_host [B,Hq,D] and seq_lens_host [B] (or NULL) to the device staging area
- * inside `workspace`, runs fd_decode, copies out/lse back to out_host /
- * lse_host (lse_host may be NULL), and synchronises `stream` before returning.
- * The KV cache (kv) stays device-resident.  Host buffers should be pinned for
- * asynchronous copies.  Workspace as for fd_decode.
+ * fd_decode with the per-step inputs and outputs in HOST memory: q_host
+ * [B,Hq,D], seq_lens_host [B] (or NULL), out_host [B,Hq,D] and lse_host
+ * [B,Hq] (or NULL).  Pinned (page-locked, device-mapped) buffers are used in
+ * place: the kernels read q and the lengths and write out and lse over the
+ * host link, with no staging copy (q_host and out_host must then start on a
+ * 16-byte boundary, else they are staged).  Pageable buffers are copied
+ * through the staging area inside `workspace` (q and lengths in, out and lse
+ * back).  Synchronises `stream` before returning, so the host may rewrite
+ * q_host and seq_lens_host as soon as the call returns.  The KV cache (kv)
+ * stays device-resident.  Workspace as for fd_decode.
  */
 FD_API fd_status fd_decode_host(const float* q_host, const fd_kv_desc* kv, float* out_host, float* lse_host,
                          int32_t B, int32_t Hq, int32_t Hkv, const int32_t* seq_lens_host,

@@ -281,13 +281,14 @@ struct HostTiles {
 // address space (cudaHostAlloc / cudaHostRegister under unified addressing);
 // false for pageable memory.  Asked on every call: a buffer freed and another
 // allocated at the same address must not inherit the old answer.
-bool host_mapped(const void* host, float** dev) {
+template <class T>
+bool host_mapped(T* host, T** dev) {
   cudaPointerAttributes a;
   void* d = nullptr;
   if (cudaPointerGetAttributes(&a, host) == cudaSuccess && a.type == cudaMemoryTypeHost && a.devicePointer)
     d = a.devicePointer;
   cudaGetLastError();  // a pageable pointer may leave an error behind on older runtimes
-  *dev = static_cast<float*>(d);
+  *dev = static_cast<T*>(d);
   return d != nullptr;
 }
 
@@ -600,20 +601,25 @@ fd_status fd_decode_host(const float* q_host, const fd_kv_desc* kv, float* out_h
   float* lse_dev = reinterpret_cast<float*>(ws + w.lse_stage);
   int32_t* len_dev = reinterpret_cast<int32_t*>(ws + w.len_stage);
   const size_t qbytes = (size_t)B * Hq * D * 4;
-  // Outputs in pinned host memory that the device can address are written by
-  // the kernels directly (no staging, no copy back); others go through the
-  // workspace and a copy.
+  // Buffers in pinned host memory that the device can address are read and
+  // written by the kernels in place, over the host link (no staging copy, no
+  // copy back: on a coherent host link that is what a copy would move, with
+  // one operation less on the stream); others go through the workspace.
   float* out_k = out_host;
   float* lse_k = lse_host;
+  const float* q_k = nullptr;
+  const int32_t* len_k = nullptr;
   if (!host_mapped(out_host, &out_k) || !aligned16(out_k)) out_k = nullptr;
   if (lse_host && !host_mapped(lse_host, &lse_k)) lse_k = nullptr;
-  if (cudaMemcpyAsync(q_dev, q_host, qbytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return FD_ERR_CUDA;
-  if (seq_lens_host &&
+  if (!host_mapped(q_host, &q_k) || !aligned16(q_k)) q_k = nullptr;
+  if (seq_lens_host && !host_mapped(seq_lens_host, &len_k)) len_k = nullptr;
+  if (!q_k && cudaMemcpyAsync(q_dev, q_host, qbytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return FD_ERR_CUDA;
+  if (seq_lens_host && !len_k &&
       cudaMemcpyAsync(len_dev, seq_lens_host, (size_t)B * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return FD_ERR_CUDA;
-  st = fd_decode(q_dev, kv, out_k ? out_k : out_dev, lse_host ? (lse_k ? lse_k : lse_dev) : nullptr, B, Hq, Hkv,
-                 seq_lens_host ? len_dev : nullptr, max_seq_len, D, scale, n_splits, workspace, workspace_bytes,
-                 stream);
+  st = fd_decode(q_k ? q_k : q_dev, kv, out_k ? out_k : out_dev, lse_host ? (lse_k ? lse_k : lse_dev) : nullptr, B,
+                 Hq, Hkv, seq_lens_host ? (len_k ? len_k : len_dev) : nullptr,
+                 max_seq_len, D, scale, n_splits, workspace, workspace_bytes, stream);
   if (st != FD_OK) return st;
   if (!out_k && cudaMemcpyAsync(out_host, out_dev, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return FD_ERR_CUDA;

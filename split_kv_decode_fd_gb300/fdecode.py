@@ -474,9 +474,9 @@ class HostDecoder:
     ``q_host`` ``[B, Hq, D]`` fp32, ``out_host`` ``[B, Hq, D]`` and ``lse_host``
     ``[B, Hq]`` (optional), ``seq_lens_host`` ``[B]`` int32 (optional) are CPU
     tensors whose contents the caller rewrites between steps; pinned buffers
-    (``pin_memory=True``) let the copies run asynchronously, and pinned outputs
-    are written by the kernels directly.  Calling the object runs one
-    synchronous step and returns ``(out_host, lse_host)``.
+    (``pin_memory=True``) are read and written by the kernels in place, over the
+    host link, and pageable ones are copied through the workspace.  Calling the
+    object runs one synchronous step and returns ``(out_host, lse_host)``.
     """
 
     def __init__(self, q_host, k, v, *, out_host=None, lse_host=None, seq_lens_host=None, max_seq_len=None,

@@ -245,26 +245,56 @@ def test_decode_host_matches_device():
     assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
 
 
-@pytest.mark.parametrize("pinned", [True, False])
-def test_host_decoder_matches_device(pinned):
-    """HostDecoder (fd_decode_host, arguments marshalled once) over several steps: pinned
-    outputs are written by the kernels directly, pageable ones come back by copy."""
+@pytest.mark.parametrize("pinned_out", [True, False])
+@pytest.mark.parametrize("pinned_in", [True, False])
+def test_host_decoder_matches_device(pinned_in, pinned_out):
+    """HostDecoder (fd_decode_host, arguments marshalled once) over several steps, the
+    caller rewriting q between them: pinned q and lengths are read and pinned outputs
+    written by the kernels in place, pageable ones go through the workspace by copy."""
     case = make_case(CONFIGS[4], "cuda")
+    q2 = case.q.flip(-1).contiguous()  # another step's q, same magnitudes
+    case2 = type(case)(case.spec, q2, case.k, case.v, case.seq_lens, case.block_table, case.max_seq_len)
     out_d, lse_d = run(case)
-    q_host = case.q.cpu().pin_memory()
-    lens_host = case.seq_lens.cpu().pin_memory()
-    out_h = torch.full((case.spec.B, case.spec.Hq, case.spec.D), float("nan"), pin_memory=pinned)
-    lse_h = torch.full((case.spec.B, case.spec.Hq), float("nan"), pin_memory=pinned)
+    out_d2, lse_d2 = run(case2)
+    torch.cuda.synchronize()
+    assert not torch.equal(out_d, out_d2)
+    q_host = torch.empty(case.q.shape, dtype=torch.float32, pin_memory=pinned_in)
+    lens_host = case.seq_lens.cpu()
+    if pinned_in:
+        lens_host = lens_host.pin_memory()
+    out_h = torch.full((case.spec.B, case.spec.Hq, case.spec.D), float("nan"), pin_memory=pinned_out)
+    lse_h = torch.full((case.spec.B, case.spec.Hq), float("nan"), pin_memory=pinned_out)
     dec = fd.HostDecoder(q_host, case.k, case.v, seq_lens_host=lens_host, max_seq_len=case.max_seq_len,
                          scale=case.spec.scale, out_host=out_h, lse_host=lse_h)
-    for step in range(3):
+    steps = ((case.q, out_d, lse_d), (q2, out_d2, lse_d2), (case.q, out_d, lse_d))
+    for step, (q_src, want_out, want_lse) in enumerate(steps):
+        q_host.copy_(q_src.cpu())
         out_h.fill_(float("nan"))
+        lse_h.fill_(float("nan"))
         o, l = dec()
         assert o is out_h and l is lse_h
-        assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu()), f"step {step}"
+        assert torch.equal(out_h, want_out.cpu()) and torch.equal(lse_h, want_lse.cpu()), f"step {step}"
     ref_out, ref_lse = oracle_for(case)
     assert_close(np64(out_h), ref_out, "out")
     assert_close(np64(lse_h), ref_lse, "lse")
+
+
+def test_decode_host_pinned_but_unaligned_q_is_staged():
+    """A pinned q that starts 4 bytes past a 16-byte boundary cannot be read in place by
+    the kernels' vector loads: fd_decode_host stages it by copy, same bits."""
+    case = make_case(CONFIGS[4], "cuda")
+    out_d, lse_d = run(case)
+    n = case.q.numel()
+    raw = torch.empty(n + 4, dtype=torch.float32, pin_memory=True)
+    q_host = raw[1:1 + n].view(case.q.shape)
+    assert q_host.data_ptr() % 16 == 4
+    q_host.copy_(case.q.cpu())
+    out_h = torch.empty((case.spec.B, case.spec.Hq, case.spec.D), pin_memory=True)
+    lse_h = torch.empty((case.spec.B, case.spec.Hq), pin_memory=True)
+    fd.decode_host(q_host, case.k, case.v, seq_lens_host=case.seq_lens.cpu().pin_memory(),
+                   max_seq_len=case.max_seq_len, scale=case.spec.scale, out_host=out_h, lse_host=lse_h)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
 
 
 def test_bad_block_table_entry_is_reported_not_faulted():
