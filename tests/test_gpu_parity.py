@@ -279,6 +279,17 @@ def test_host_decoder_matches_device(pinned_in, pinned_out):
     assert_close(np64(lse_h), ref_lse, "lse")
 
 
+def test_host_decoder_without_lse():
+    """lse_host omitted: fd_decode_host gets NULL and writes out only, same bits."""
+    case = make_case(CONFIGS[4], "cuda")
+    out_d, _ = run(case)
+    dec = fd.HostDecoder(case.q.cpu().pin_memory(), case.k, case.v, seq_lens_host=case.seq_lens.cpu().pin_memory(),
+                         max_seq_len=case.max_seq_len, scale=case.spec.scale)
+    out_h, lse_h = dec()
+    assert lse_h is None
+    assert torch.equal(out_h, out_d.cpu())
+
+
 def test_decode_host_pinned_but_unaligned_q_is_staged():
     """A pinned q that starts 4 bytes past a 16-byte boundary cannot be read in place by
     the kernels' vector loads: fd_decode_host stages it by copy, same bits."""
