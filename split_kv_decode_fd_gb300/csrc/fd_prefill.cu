@@ -250,6 +250,40 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// Two fp32 values in one 64-bit register (x in the low half) and the sm_100
+// family's packed fp32 add / subtract, which round each half as the scalar
+// instruction does: one instruction for two keys in the softmax.
+__device__ __forceinline__ uint64_t f2_pack(float x, float y) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(x), "f"(y));
+  return d;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& x, float& y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// split2 on a packed pair (p = {x0, x1}): the same roundings, the residual
+// taken by one packed subtract.
+__device__ __forceinline__ void split2x(float x0, float x1, uint64_t p, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const uint32_t hb = *reinterpret_cast<const uint32_t*>(&h);
+  float r0, r1;
+  f2_unpack(f2_sub(p, f2_pack(__uint_as_float(hb << 16), __uint_as_float(hb & 0xffff0000u))), r0, r1);
+  const __nv_bfloat162 r = __floats2bfloat162_rn(r0, r1);
+  hi = hb;
+  lo = *reinterpret_cast<const uint32_t*>(&r);
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -797,20 +831,29 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         // (16 keys) at a time: k-step kk's hi in columns 16 kk + [0, 8), its lo in
         // 16 kk + [8, 16), two keys per column.  The whole tile's S is in
         // registers already, so the stores may overwrite any of it.
+        // Keys go in pairs through the packed fp32 instructions: four running
+        // sums, keys 4i and 4i+1 into the first pair, 4i+2 and 4i+3 into the
+        // second.
         const float base = mref == -INFINITY ? 0.f : mref;
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint64_t base2 = f2_pack(base, base);
+        uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < kN / 16; ++c) {
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float p0 = ex2(s[16 * c + 2 * e] - base), p1 = ex2(s[16 * c + 2 * e + 1] - base);
-            sum4[(2 * e) & 3] += p0;
-            sum4[(2 * e + 1) & 3] += p1;
-            split2(p0, p1, w[e], w[8 + e]);
+            float t0, t1;
+            f2_unpack(f2_sub(f2_pack(s[16 * c + 2 * e], s[16 * c + 2 * e + 1]), base2), t0, t1);
+            const float p0 = ex2(t0), p1 = ex2(t1);
+            const uint64_t p2 = f2_pack(p0, p1);
+            sum2[e & 1] = f2_add(sum2[e & 1], p2);
+            split2x(p0, p1, p2, w[e], w[8 + e]);
           }
           tmem_st16u(tbase + (uint32_t)c * 16u, w);
         }
+        float sum4[4];
+        f2_unpack(sum2[0], sum4[0], sum4[1]);
+        f2_unpack(sum2[1], sum4[2], sum4[3]);
         l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
         // Rescaling O needs the previous tile's P.V to have finished.  With two
         // heads it was issued before this tile's S, whose completion this group
