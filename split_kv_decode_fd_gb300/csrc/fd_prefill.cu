@@ -250,6 +250,14 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// max of three (the sm_100 family's three-input max: a NaN input is ignored,
+// as fmaxf ignores it).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Two fp32 values in one 64-bit register (x in the low half) and the sm_100
 // family's packed fp32 add / subtract, which round each half as the scalar
 // instruction does: one instruction for two keys in the softmax.
@@ -818,8 +826,10 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         }
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < kN; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        for (int c = 0; c < kN; c += 8)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mx4[i] = fmax3(mx4[i], s[c + 2 * i], s[c + 2 * i + 1]);
+        const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
         const bool rescale = mx > mref + kTau;
         float alpha = 1.f;
         if (rescale) {
