@@ -280,15 +280,18 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
   return d;
 }
 
-// split2 on a packed pair (p = {x0, x1}): the same roundings, the residual
-// taken by one packed subtract.
+// x = hi + lo for a packed pair (p = {x0, x1}, x0's parts in the low
+// halves), for P: hi is x truncated to bf16 (the upper 16 bits, one byte
+// permute for both), the residual x - hi is exact in fp32 (one packed
+// subtract) and lo is its bf16 rounding.  |lo| < 2^-7 |x| and lo is good to
+// 2^-9 of itself, so hi + lo holds x to 2^-16, with an unbiased error; the
+// rounding conversion that split2 uses for hi measured 3 % slower here.
 __device__ __forceinline__ void split2x(float x0, float x1, uint64_t p, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const uint32_t hb = *reinterpret_cast<const uint32_t*>(&h);
+  const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+  hi = __byte_perm(b0, b1, 0x7632);
   float r0, r1;
-  f2_unpack(f2_sub(p, f2_pack(__uint_as_float(hb << 16), __uint_as_float(hb & 0xffff0000u))), r0, r1);
+  f2_unpack(f2_sub(p, f2_pack(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u))), r0, r1);
   const __nv_bfloat162 r = __floats2bfloat162_rn(r0, r1);
-  hi = hb;
   lo = *reinterpret_cast<const uint32_t*>(&r);
 }
 
