@@ -70,6 +70,7 @@ constexpr int kRegsHigh = 208;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads<1> * kLaunchRegs, "register split exceeds the pool");
 static_assert(kRegsLow + 2 * kRegsHigh <= 512, "one warp of each group per sub-partition: 16384 registers");
 constexpr float kTau = 8.0f;
+constexpr float kSumFast = 128.0f;  // 2^(tau - 1): see the softmax
 constexpr float kLn2f = 0.6931471805599453f;
 constexpr uint32_t kTmemCols = 512;  // per head (256 each): S / P at +0, O (D columns) at +128
 
@@ -827,47 +828,65 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
 #pragma unroll
           for (int c = 0; c < kN; ++c) s[c] = c < keys_left ? s[c] : -INFINITY;
         }
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < kN; c += 8)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) mx4[i] = fmax3(mx4[i], s[c + 2 * i], s[c + 2 * i + 1]);
-        const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
-        const bool rescale = mx > mref + kTau;
-        float alpha = 1.f;
-        if (rescale) {
-          const float mn = fmaxf(mref, mx);
-          alpha = mref == -INFINITY ? 0.f : ex2(mref - mn);
-          mref = mn;
-        }
-        // p = 2^(s - max) and its bf16 hi / lo over the same columns, one k-step
+        // p = 2^(s - base) and its bf16 hi / lo over the same columns, one k-step
         // (16 keys) at a time: k-step kk's hi in columns 16 kk + [0, 8), its lo in
         // 16 kk + [8, 16), two keys per column.  The whole tile's S is in
-        // registers already, so the stores may overwrite any of it.
-        // Keys go in pairs through the packed fp32 instructions: four running
-        // sums, keys 4i and 4i+1 into the first pair, 4i+2 and 4i+3 into the
-        // second.
-        const float base = mref == -INFINITY ? 0.f : mref;
-        const uint64_t base2 = f2_pack(base, base);
-        uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+        // registers already, so the stores may overwrite any of it.  Keys go in
+        // pairs through the packed fp32 instructions: four running sums, keys 4i
+        // and 4i+1 into the first pair, 4i+2 and 4i+3 into the second.  Returns
+        // the row's sum of p.  Warp-collective (the TMEM stores).
+        auto make_p = [&](float base) -> float {
+          const uint64_t base2 = f2_pack(base, base);
+          uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
-        for (int c = 0; c < kN / 16; ++c) {
-          uint32_t w[16];
+          for (int c = 0; c < kN / 16; ++c) {
+            uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float t0, t1;
-            f2_unpack(f2_sub(f2_pack(s[16 * c + 2 * e], s[16 * c + 2 * e + 1]), base2), t0, t1);
-            const float p0 = ex2(t0), p1 = ex2(t1);
-            const uint64_t p2 = f2_pack(p0, p1);
-            sum2[e & 1] = f2_add(sum2[e & 1], p2);
-            split2x(p0, p1, p2, w[e], w[8 + e]);
+            for (int e = 0; e < 8; ++e) {
+              float t0, t1;
+              f2_unpack(f2_sub(f2_pack(s[16 * c + 2 * e], s[16 * c + 2 * e + 1]), base2), t0, t1);
+              const float p0 = ex2(t0), p1 = ex2(t1);
+              const uint64_t p2 = f2_pack(p0, p1);
+              sum2[e & 1] = f2_add(sum2[e & 1], p2);
+              split2x(p0, p1, p2, w[e], w[8 + e]);
+            }
+            tmem_st16u(tbase + (uint32_t)c * 16u, w);
           }
-          tmem_st16u(tbase + (uint32_t)c * 16u, w);
+          float sum4[4];
+          f2_unpack(sum2[0], sum4[0], sum4[1]);
+          f2_unpack(sum2[1], sum4[2], sum4[3]);
+          return (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        };
+        // The running max moves (and O and l are rescaled) only when the tile's
+        // max exceeds it by more than tau.  Once a row has a finite running max,
+        // P is first made with it as the base: a sum of p below 2^(tau-1) means
+        // that no key came within one of tau above it, so the max would not have
+        // moved and P and the sum are exactly what the max-first order gives,
+        // without the 128-key max.  Otherwise (a larger or NaN sum, the first
+        // keys of a row) the warp takes the max-first order, P made again.
+        bool rescale = false;
+        float alpha = 1.f, psum = 0.f;
+        bool slow = true;
+        if (__any_sync(0xffffffffu, mref != -INFINITY)) {
+          psum = make_p(mref != -INFINITY ? mref : 0.f);
+          slow = mref == -INFINITY || !(psum < kSumFast);
         }
-        float sum4[4];
-        f2_unpack(sum2[0], sum4[0], sum4[1]);
-        f2_unpack(sum2[1], sum4[2], sum4[3]);
-        l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+        if (__any_sync(0xffffffffu, slow)) {
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int c = 0; c < kN; c += 8)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mx4[i] = fmax3(mx4[i], s[c + 2 * i], s[c + 2 * i + 1]);
+          const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
+          rescale = mx > mref + kTau;
+          if (rescale) {
+            const float mn = fmaxf(mref, mx);
+            alpha = mref == -INFINITY ? 0.f : ex2(mref - mn);
+            mref = mn;
+          }
+          psum = make_p(mref == -INFINITY ? 0.f : mref);
+        }
+        l = l * alpha + psum;
         // Rescaling O needs the previous tile's P.V to have finished.  With two
         // heads it was issued before this tile's S, whose completion this group
         // just saw; with one head it comes after, and o_done tells (a parity
