@@ -242,15 +242,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// x = hi + lo in bf16, packed as a pair (x0's part in the low half).
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 r = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&r);
-}
-
 // max of three (the sm_100 family's three-input max: a NaN input is ignored,
 // as fmaxf ignores it).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -260,8 +251,8 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 // Two fp32 values in one 64-bit register (x in the low half) and the sm_100
-// family's packed fp32 add / subtract, which round each half as the scalar
-// instruction does: one instruction for two keys in the softmax.
+// family's packed fp32 add / subtract / multiply, which round each half as the
+// scalar instruction does: one instruction for two keys in the softmax.
 __device__ __forceinline__ uint64_t f2_pack(float x, float y) {
   uint64_t d;
   asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(x), "f"(y));
@@ -275,10 +266,28 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
+}
+
+// x = hi + lo in bf16 for a packed pair (p = {x0, x1}, x0's parts in the low
+// halves), for q: both rounded to nearest, the residual x - hi (exact in fp32)
+// by one packed subtract.
+__device__ __forceinline__ void split2_rn(float x0, float x1, uint64_t p, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const uint32_t hb = *reinterpret_cast<const uint32_t*>(&h);
+  float r0, r1;
+  f2_unpack(f2_sub(p, f2_pack(__uint_as_float(hb << 16), __uint_as_float(hb & 0xffff0000u))), r0, r1);
+  const __nv_bfloat162 r = __floats2bfloat162_rn(r0, r1);
+  hi = hb;
+  lo = *reinterpret_cast<const uint32_t*>(&r);
 }
 
 // x = hi + lo for a packed pair (p = {x0, x1}, x0's parts in the low
@@ -286,8 +295,8 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
 // permute for both), the residual x - hi is exact in fp32 (one packed
 // subtract) and lo is its bf16 rounding.  |lo| < 2^-7 |x| and lo is good to
 // 2^-9 of itself, so hi + lo holds x to 2^-16, with an unbiased error; the
-// rounding conversion that split2 uses for hi measured 3 % slower here.
-__device__ __forceinline__ void split2x(float x0, float x1, uint64_t p, uint32_t& hi, uint32_t& lo) {
+// rounding conversion of split2_rn measured 3 % slower here.
+__device__ __forceinline__ void split2_trunc(float x0, float x1, uint64_t p, uint32_t& hi, uint32_t& lo) {
   const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
   hi = __byte_perm(b0, b1, 0x7632);
   float r0, r1;
@@ -773,12 +782,18 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
           }
         };
         // columns [64h, 64h+64) from v[64] -> hi block h, lo block kNB + h
+        const uint64_t scale2 = f2_pack(p.qk_scale, p.qk_scale);
         auto store64 = [&](int hb, const float* v) {
 #pragma unroll
           for (int c = 0; c < 64; c += 4) {
             uint32_t hi0, lo0, hi1, lo1;
-            split2(v[c] * p.qk_scale, v[c + 1] * p.qk_scale, hi0, lo0);
-            split2(v[c + 2] * p.qk_scale, v[c + 3] * p.qk_scale, hi1, lo1);
+            const uint64_t x01 = f2_mul(f2_pack(v[c], v[c + 1]), scale2);
+            const uint64_t x23 = f2_mul(f2_pack(v[c + 2], v[c + 3]), scale2);
+            float x0, x1, x2, x3;
+            f2_unpack(x01, x0, x1);
+            f2_unpack(x23, x2, x3);
+            split2_rn(x0, x1, x01, hi0, lo0);
+            split2_rn(x2, x3, x23, hi1, lo1);
             const uint32_t off = (uint32_t)hb * 16384u + swz((uint32_t)r, (uint32_t)(c >> 3)) + (uint32_t)((c >> 2) & 1) * 8u;
             sts64(qbase + kQhi + off, hi0, hi1);
             sts64(qbase + kQlo + off, lo0, lo1);
@@ -848,7 +863,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
               const float p0 = ex2(t0), p1 = ex2(t1);
               const uint64_t p2 = f2_pack(p0, p1);
               sum2[e & 1] = f2_add(sum2[e & 1], p2);
-              split2x(p0, p1, p2, w[e], w[8 + e]);
+              split2_trunc(p0, p1, p2, w[e], w[8 + e]);
             }
             tmem_st16u(tbase + (uint32_t)c * 16u, w);
           }
@@ -939,16 +954,22 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         // with the 128-byte swizzle, then out with tensor stores of 32 columns x
         // 128 rows, which leave the rows past n_q alone.  (Measured: 4k prompt
         // -3 %; with one head per CTA, whose CTAs are short, direct stores.)
-#pragma unroll 1
+        // the row's D columns in one batch of TMEM loads, then scaled in pairs
+        float o[kD];
+#pragma unroll
+        for (int c4 = 0; c4 < kD / 32; ++c4) tmem_ld32_nw(obase + (uint32_t)c4 * 32, o + 32 * c4);
+        tmem_wait_ld();
+        const uint64_t inv2 = f2_pack(inv, inv);
+#pragma unroll
         for (int c4 = 0; c4 < kD / 32; ++c4) {
-          float o[32];
-          tmem_ld32(obase + (uint32_t)c4 * 32, o);
           const uint32_t blk = qbase + (uint32_t)c4 * kBlockBytes;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            sts128(blk + swz((uint32_t)r, (uint32_t)c), __float_as_uint(o[4 * c] * inv),
-                   __float_as_uint(o[4 * c + 1] * inv), __float_as_uint(o[4 * c + 2] * inv),
-                   __float_as_uint(o[4 * c + 3] * inv));
+          for (int c = 0; c < 8; ++c) {
+            const int i = 32 * c4 + 4 * c;
+            const uint64_t a = f2_mul(f2_pack(o[i], o[i + 1]), inv2), b = f2_mul(f2_pack(o[i + 2], o[i + 3]), inv2);
+            sts128(blk + swz((uint32_t)r, (uint32_t)c), (uint32_t)a, (uint32_t)(a >> 32), (uint32_t)b,
+                   (uint32_t)(b >> 32));
+          }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the staged rows, for the tensor stores
         named_barrier(1 + G, 128);
