@@ -37,7 +37,9 @@
 // scale*log2 e) and p are split into bf16 hi + lo parts and each product is
 // issued twice (hi, then lo) into the same fp32 accumulator -- two MMAs buy
 // fp32-level accuracy.  The online softmax rescales lazily: the reference max
-// moves only when a score exceeds it by kTau (base 2), so p <= 2^kTau.
+// moves only when a score exceeds it by kTau (base 2), so p <= 2^kTau; the
+// softmax's arithmetic goes two keys per instruction (packed fp32), which is
+// what its time per tile, and with it the steady state, depends on.
 #include <cuda_bf16.h>
 
 #include "fd_device.cuh"
@@ -834,8 +836,9 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         if (lane == 0) mbar_arrive(q_ready);
       }
 
-      // A failed wait never leaves the loop early (the named barrier below needs
-      // all 128 threads of the group): later waits are skipped, the output flagged.
+      // A failed wait never leaves the loop early (the epilogue's named barrier
+      // needs all 128 threads of the group): later waits are skipped, the output
+      // flagged.
       float mref = -INFINITY, l = 0.f;
       for (int32_t j = 0; j < n; ++j) {
         const uint32_t gj = g + (uint32_t)j;
