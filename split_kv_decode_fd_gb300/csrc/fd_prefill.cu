@@ -961,6 +961,10 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
       if (n > 0) {
         if (ok && !bar_ok(o_final + G, f & 1, abort_flag, wl)) ok = false;
         tc_fence_after();
+        // Every S MMA of the item has completed.  With one head per CTA the
+        // epilogue stores its rows directly and leaves the q area alone, so the
+        // next item's q may load into it while the stores run (MHA 4k -1.3 %).
+        if (NG == 1 && warp == kSoftmax0<NG> + 4 * G && lane == 0) mbar_arrive(q_free);
       }
       const float inv = l > 0.f && ok ? 1.f / l : 0.f;
       if (NG == 2 && n > 0) {
@@ -968,7 +972,9 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         // item has completed before its last P.V): [D/32 blocks][128 rows][128 B]
         // with the 128-byte swizzle, then out with tensor stores of 32 columns x
         // 128 rows, which leave the rows past n_q alone.  (Measured: 4k prompt
-        // -3 %; with one head per CTA, whose CTAs are short, direct stores.)
+        // -3 %; direct stores here, even with the q area released at the last
+        // MMA for the next q, +4 %.  With one head per CTA, whose CTAs are
+        // short, direct stores.)
         // the row's D columns in one batch of TMEM loads, then scaled in pairs
         float o[kD];
 #pragma unroll
@@ -1015,8 +1021,6 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
                   make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
           }
         }
-        // every S MMA of the item has completed (o_final): the q area may take the next q
-        if (n > 0 && warp == kSoftmax0<NG> + 4 * G && lane == 0) mbar_arrive(q_free);
       }
       if (qi < p.n_q && p.lse)
         p.lse[((size_t)it.b * p.Hq + h) * p.n_q + qi] = l > 0.f ? (mref + log2f(l)) * kLn2f : -INFINITY;
