@@ -425,13 +425,16 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
   uint64_t* s_full = bars + 16;    // [2 buffers]
   uint64_t* p_full = bars + 18;    // [2 buffers]
   uint64_t* o_final = bars + 20;   // [2 heads]: an item's last P.V has completed
-  uint64_t* q_ready = bars + 22;   // an item's q tiles are in shared memory
   uint64_t* drain = bars + 23;
   uint64_t* o_done = bars + 24;    // one head per CTA only: a P.V has completed
-  uint64_t* q_full = bars + 25;    // an item's q tiles (fp32) have landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 208);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 212);
-  uint64_t* q_free = bars + 27;    // the q areas may take the next item's q (one arrival per head)
+  // Each head's q area has barriers of its own, so that head 0 takes its next
+  // item's q while head 1 still finishes the current item (its last P.V is
+  // the CTA's last MMA).
+  uint64_t* q_full = bars + 34;    // [2 heads]: the item's q tiles (fp32) have landed
+  uint64_t* q_ready = bars + 36;   // [2 heads]: ... and are bf16 hi / lo
+  uint64_t* q_free = bars + 38;    // [2 heads]: the q area may take the next item's q
   // The item queue: the producer takes item indices from a global counter and
   // hands them to the other roles through two slots (index -1 = no more items).
   uint64_t* item_full = bars + 28;   // [2]
@@ -460,11 +463,13 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
       mbar_init(p_full + i, 4);
       mbar_init(o_final + i, 1);
     }
-    mbar_init(q_ready, 4 * ngroups);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(q_full + i, 1);
+      mbar_init(q_ready + i, 4);
+      mbar_init(q_free + i, 1);
+    }
     mbar_init(drain, 1);
     mbar_init(o_done, 1);
-    mbar_init(q_full, 1);
-    mbar_init(q_free, ngroups);
     for (int i = 0; i < 2; ++i) {
       mbar_init(item_full + i, 1);
       mbar_init(item_empty + i, 1 + 4 * ngroups);
@@ -499,7 +504,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
     // ------------------------------------------------------------ producer
     regs_dec<NG, kRegsLow>();
     uint32_t u = 0;   // slot uses so far
-    uint32_t fq = 0;  // items with key tiles whose q this warp has loaded
+    uint32_t fq[2] = {0u, 0u};  // per head: items with key tiles whose q this warp has loaded
     uint32_t stalled = 0xffffffffu;  // the copy skipped by the testing hook
     Ring pr;          // the next use's slot
     for (uint32_t e = 0;; ++e) {
@@ -528,22 +533,23 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
       if (idx < 0) break;
       const Item it = item_of(p, idx, ngroups, n_m);
       if (it.n_tiles > 0) {
-        // the item's q tiles, fp32, into the heads' q areas (the softmax groups
-        // convert them there), once the previous item is done with those areas
-        if (lane == 0) {
-          if (fq > 0 && !bar_ok(q_free, (fq - 1) & 1u, abort_flag, wl)) ok = false;
-          if (ok) {
-            mbar_arrive_expect_tx(q_full, (uint32_t)(ngroups * kD * kM * 4));
+        // the item's q tiles, fp32, into each head's q area (the softmax group
+        // converts them there), once the head's previous item is done with it
 #pragma unroll
-            for (int G = 0; G < ngroups; ++G)
+        for (int G = 0; G < ngroups; ++G) {
+          if (lane == 0) {
+            if (ok && fq[G] > 0 && !bar_ok(q_free + G, (fq[G] - 1) & 1u, abort_flag, wl)) ok = false;
+            if (ok) {
+              mbar_arrive_expect_tx(q_full + G, (uint32_t)(kD * kM * 4));
 #pragma unroll
               for (int blk = 0; blk < kD / 32; ++blk)
-                tma_load_3d(smem + (uint32_t)G * kQGroupBytes + (uint32_t)blk * kBlockBytes, &tmap_q, q_full, blk * 32,
-                            it.m0, it.b * p.Hq + it.h0 + G);
+                tma_load_3d(smem + (uint32_t)G * kQGroupBytes + (uint32_t)blk * kBlockBytes, &tmap_q, q_full + G,
+                            blk * 32, it.m0, it.b * p.Hq + it.h0 + G);
+            }
           }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (ok) ++fq[G];
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) ++fq;
       }
       for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
         // lane l brings rows [16 l, 16 l + 16) of the tile: one page run when paged
@@ -590,7 +596,9 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
       const uint32_t first = u > nslots ? u - nslots : 0;
       for (uint32_t t = first; t < u; ++t)
         if (t != stalled && !mbar_wait_for(kv_full + t % nslots, (t / nslots) & 1, wl)) atomicOr(p.err, kErrTimeout);
-      if (fq > 0 && !mbar_wait_for(q_full, (fq - 1) & 1u, wl)) atomicOr(p.err, kErrTimeout);
+#pragma unroll
+      for (int G = 0; G < ngroups; ++G)
+        if (fq[G] > 0 && !mbar_wait_for(q_full + G, (fq[G] - 1) & 1u, wl)) atomicOr(p.err, kErrTimeout);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -649,7 +657,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         const Item it = item_of(p, idx, ngroups, n_m);
         const int32_t n = it.n_tiles;
         if (n == 0) continue;  // no q_ready phase either: the softmax skips such items too
-        if (!wait_ok(q_ready, f & 1, abort_flag, wl)) {
+        if (!wait_ok(q_ready + 0, f & 1, abort_flag, wl)) {
           ok = false;
           break;
         }
@@ -672,6 +680,10 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
               }
               issue_pv(256, 384, vprev.slot, j == 1);
               umma_commit(kv_empty + vprev.slot);
+            } else if (!wait_ok(q_ready + 1, f & 1, abort_flag, wl)) {
+              // head 1's q, at the item's first tile
+              ok = false;
+              break;
             }
             issue_s(256, 1, kr.slot);
             umma_commit(s_full + 1);
@@ -781,8 +793,8 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         // fp32 columns [32b, 32b+32) sit in block b, the hi of columns
         // [64h, 64h+64) in block h and their lo in block D/64 + h; a block is
         // read before it is written.  The previous item is done with this area
-        // (the producer waited for q_free before the loads).
-        if (ok && !bar_ok(q_full, f & 1, abort_flag, wl)) ok = false;
+        // (the producer waited for the head's q_free before the loads).
+        if (ok && !bar_ok(q_full + G, f & 1, abort_flag, wl)) ok = false;
         auto load32 = [&](int blk, float* v) {
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -833,7 +845,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(q_ready);
+        if (lane == 0) mbar_arrive(q_ready + G);
       }
 
       // A failed wait never leaves the loop early (the epilogue's named barrier
@@ -964,7 +976,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
         // Every S MMA of the item has completed.  With one head per CTA the
         // epilogue stores its rows directly and leaves the q area alone, so the
         // next item's q may load into it while the stores run (MHA 4k -1.3 %).
-        if (NG == 1 && warp == kSoftmax0<NG> + 4 * G && lane == 0) mbar_arrive(q_free);
+        if (NG == 1 && warp == kSoftmax0<NG> + 4 * G && lane == 0) mbar_arrive(q_free + G);
       }
       const float inv = l > 0.f && ok ? 1.f / l : 0.f;
       if (NG == 2 && n > 0) {
@@ -1000,7 +1012,7 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
             tma_store_3d(&tmap_o, qbase + (uint32_t)c4 * kBlockBytes, c4 * 32, it.m0, it.b * p.Hq + h);
           bulk_commit_group();
           bulk_wait_read_all();  // the q area is free again (and the CTA may exit)
-          mbar_arrive(q_free);
+          mbar_arrive(q_free + G);
         }
       } else {
         // one head per CTA (short CTAs), or an item without keys: direct stores
