@@ -10,8 +10,7 @@
 //
 // Work item: (batch, pair of query heads of one GQA group -- or one head when
 // the group size is odd --, tile of kPrefillRows = 128 query rows), taken
-// longest first; a CTA per item, or with two heads a CTA per SM taking items
-// from a queue.  Ten warps
+// longest first by one CTA per SM from a queue (a global counter).  Ten warps
 // (twelve with one head per CTA: warps 2 and 3 have no role there, and the
 // softmax groups are warps 4-7 and 8-11):
 //   warp 0    TMA producer: 128-key K tiles and V tiles (16-row x 128-byte
@@ -450,8 +449,8 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
   constexpr uint32_t nslots = NG == 2 ? (uint32_t)Lay::kSlots : (uint32_t)Lay::kSlotsOneHead;
   const int32_t n_m = (p.n_q + kM - 1) / kM;
   const int32_t n_items = n_m * (p.Hq / ngroups) * p.B;
-  // persistent CTAs taking items from p.work (two heads per CTA only)
-  const bool queue = NG == 2 && (int32_t)gridDim.x < n_items;
+  // persistent CTAs taking items from p.work
+  const bool queue = (int32_t)gridDim.x < n_items;
 
   if (tid == 0) {
     for (uint32_t i = 0; i < nslots; ++i) {
@@ -510,26 +509,21 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
     for (uint32_t e = 0;; ++e) {
       // take the next item (longest first) and announce it; -1 ends the walk
       int32_t idx = -1;
-      if constexpr (NG == 2) {
-        if (lane == 0) {
-          const uint32_t sl = e & 1u;
-          if (e >= 2 && ok && !bar_ok(item_empty + sl, ((e >> 1) & 1u) ^ 1u, abort_flag, wl)) ok = false;
-          if (ok) {
-            // the first item is the CTA's own; then, with fewer CTAs than items,
-            // the next one not yet taken
-            const int32_t t = e == 0 ? (int32_t)blockIdx.x
-                                     : (queue ? (int32_t)gridDim.x + (int32_t)atomicAdd(p.work, 1u) : n_items);
-            idx = t < n_items ? t : -1;
-          }
-          item_slot[sl] = idx;
-          mbar_arrive(item_full + sl);
+      if (lane == 0) {
+        const uint32_t sl = e & 1u;
+        if (e >= 2 && ok && !bar_ok(item_empty + sl, ((e >> 1) & 1u) ^ 1u, abort_flag, wl)) ok = false;
+        if (ok) {
+          // the first item is the CTA's own; then, with fewer CTAs than items,
+          // the next one not yet taken
+          const int32_t t = e == 0 ? (int32_t)blockIdx.x
+                                   : (queue ? (int32_t)gridDim.x + (int32_t)atomicAdd(p.work, 1u) : n_items);
+          idx = t < n_items ? t : -1;
         }
-        idx = __shfl_sync(0xffffffffu, idx, 0);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-      } else {
-        const int64_t t = (int64_t)blockIdx.x + (int64_t)e * gridDim.x;
-        idx = t < n_items && ok ? (int32_t)t : -1;
+        item_slot[sl] = idx;
+        mbar_arrive(item_full + sl);
       }
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
       if (idx < 0) break;
       const Item it = item_of(p, idx, ngroups, n_m);
       if (it.n_tiles > 0) {
@@ -640,19 +634,13 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
       };
       Ring kr;  // K of the next tile
       for (uint32_t e = 0;; ++e) {
-        int32_t idx;
-        if constexpr (NG == 2) {
-          const uint32_t sl = e & 1u;
-          if (!wait_ok(item_full + sl, (e >> 1) & 1u, abort_flag, wl)) {
-            ok = false;
-            break;
-          }
-          idx = item_slot[sl];
-          mbar_arrive(item_empty + sl);
-        } else {
-          const int64_t t = (int64_t)blockIdx.x + (int64_t)e * gridDim.x;
-          idx = t < n_items ? (int32_t)t : -1;
+        const uint32_t sl = e & 1u;
+        if (!wait_ok(item_full + sl, (e >> 1) & 1u, abort_flag, wl)) {
+          ok = false;
+          break;
         }
+        const int32_t idx = item_slot[sl];
+        mbar_arrive(item_empty + sl);
         if (idx < 0 || !ok) break;
         const Item it = item_of(p, idx, ngroups, n_m);
         const int32_t n = it.n_tiles;
@@ -767,17 +755,12 @@ __global__ void __launch_bounds__(kThreads<NG>, 1)
     uint32_t g = 0, f = 0;
     for (uint32_t e = 0;; ++e) {
       int32_t idx = -1;
-      if constexpr (NG == 2) {
-        if (lane == 0) {
-          const uint32_t sl = e & 1u;
-          if (bar_ok(item_full + sl, (e >> 1) & 1u, abort_flag, wl)) idx = item_slot[sl];
-          mbar_arrive(item_empty + sl);
-        }
-        idx = __shfl_sync(0xffffffffu, idx, 0);
-      } else {
-        const int64_t t = (int64_t)blockIdx.x + (int64_t)e * gridDim.x;
-        idx = t < n_items ? (int32_t)t : -1;
+      if (lane == 0) {
+        const uint32_t sl = e & 1u;
+        if (bar_ok(item_full + sl, (e >> 1) & 1u, abort_flag, wl)) idx = item_slot[sl];
+        mbar_arrive(item_empty + sl);
       }
+      idx = __shfl_sync(0xffffffffu, idx, 0);
       if (idx < 0) break;  // every warp of the group reads the same slot, so all leave together
       const Item it = item_of(p, idx, ngroups, n_m);
       const int32_t n = it.n_tiles;
@@ -1082,9 +1065,6 @@ cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const
     if (e != cudaSuccess) return e;
     configured = dev;
   }
-  // One CTA per item, items numbered longest first: the hardware hands the next
-  // item to whichever SM frees up (measured faster than persistent CTAs taking
-  // items round-robin, whose tails do not even out).
   const int64_t items = (int64_t)((p.n_q + kM - 1) / kM) * (p.Hq / NG) * p.B;
   if (items > 0x7FFFFFFF) return cudaErrorInvalidValue;
   static int sms = 0, sms_dev = -1;
@@ -1093,12 +1073,12 @@ cudaError_t launch_prefill_t(const CUtensorMap& tk, const CUtensorMap& tv, const
     if (e != cudaSuccess) return e;
     sms_dev = dev;
   }
-  // Two heads per CTA: one CTA per SM, each taking the next longest-first item
-  // from a global counter as it finishes one, so that the next item's q and K/V
-  // load while the current one ends (4k prompt -1.5 %, 16k -0.7 %).  One head
-  // per CTA: a CTA per item, handed out by the hardware in index order (the
-  // queue measured +1.6 % / +3.6 % there).
-  const dim3 grid((unsigned)(NG == 2 && items > sms ? sms : items));
+  // One CTA per SM, each taking the next longest-first item from a global
+  // counter as it finishes one, so that the next item's q and K/V load while
+  // the current one ends (4k prompt: two heads per CTA -1.5 %, one head -3.7 %;
+  // a CTA per item handed out by the hardware, and persistent CTAs walking a
+  // fixed order, measured slower).
+  const dim3 grid((unsigned)(items > sms ? sms : items));
   fd_prefill_kernel<D, NG, kHook><<<grid, kThreads<NG>, PLayout<D>::kSmemAlloc, stream>>>(tk, tv, tq, to, p);
   return cudaGetLastError();
 }

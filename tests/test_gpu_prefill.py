@@ -210,10 +210,9 @@ def test_prefill_writes_only_its_rows(hq, hkv, d):
                          ids=["two_heads_per_cta", "one_head_per_cta", "two_heads_d64", "two_heads_paged16",
                               "two_heads_paged64"])
 def test_prefill_more_items_than_sms(hq, hkv, B, n_q, d, layout, page):
-    """More 128-row query tiles than SMs: with two heads per CTA the CTAs take
-    items from the queue, with one head they run in waves; sequences without
-    keys among them, contiguous and paged caches: every output matches the
-    oracle."""
+    """More 128-row query tiles than SMs: one CTA per SM takes the items from
+    the queue, with two heads or one head per CTA; sequences without keys among
+    them, contiguous and paged caches: every output matches the oracle."""
     spec = small_spec("many_items", B, hq, hkv, d, 1400, layout=layout, page_size=page, seed=33)
     lengths = [0, 800, 650, 700, 720, 0, 790, 800] if B > 2 else [1400, 0]
     case = make_case(spec, "cuda", lengths=lengths)
@@ -225,11 +224,13 @@ def test_prefill_more_items_than_sms(hq, hkv, B, n_q, d, layout, page):
     assert_close(np64(lse), ref_lse, "lse")
 
 
-def test_prefill_queue_counters_return_to_zero():
-    """With two heads per CTA and more query tiles than SMs, CTAs take items from
-    two counters in the workspace header (bytes 128-135): the last CTA leaves
-    both at zero, and the results do not depend on which CTA took which item."""
-    spec = small_spec("queue", 2, 32, 8, 128, 1300, seed=35)
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (12, 4)], ids=["two_heads_per_cta", "one_head_per_cta"])
+def test_prefill_queue_counters_return_to_zero(hq, hkv):
+    """With more query tiles than SMs, CTAs take items from two counters in the
+    workspace header (bytes 128-135): the last CTA leaves both at zero, and the
+    results do not depend on which CTA took which item (two heads per CTA, and
+    one head for an odd group size)."""
+    spec = small_spec("queue", 2, hq, hkv, 128, 1300, seed=35)
     case = make_case(spec, "cuda", lengths=[1300, 1290])
     q = window_q(case, 1280, seed=15)
     ws = fd.Workspace()

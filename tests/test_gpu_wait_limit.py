@@ -43,8 +43,9 @@ def test_wait_that_runs_out_is_reported_and_the_next_call_is_clean(n_splits, sta
 
 
 @pytest.mark.parametrize("hq,hkv,B,n_q,stage", [(8, 2, 2, 300, 0), (8, 2, 2, 300, 3), (6, 2, 2, 300, 1),
-                                                (32, 8, 2, 1280, 3)],
-                         ids=["two_heads_first_copy", "two_heads_fourth_copy", "one_head", "queue"])
+                                                (32, 8, 2, 1280, 3), (12, 4, 2, 1280, 2)],
+                         ids=["two_heads_first_copy", "two_heads_fourth_copy", "one_head", "queue",
+                              "one_head_queue"])
 def test_prefill_wait_that_runs_out_is_reported_and_the_next_call_is_clean(hq, hkv, B, n_q, stage):
     """The prefill kernel's waits are bounded the same way: with one K/V copy
     skipped in every CTA (two heads per CTA, one head, and the persistent
