@@ -206,20 +206,23 @@ def test_prefill_writes_only_its_rows(hq, hkv, d):
                                                        (6, 2, 8, 512, 128, "contiguous", 16),
                                                        (32, 8, 2, 1280, 64, "contiguous", 16),
                                                        (32, 8, 2, 1280, 128, "paged", 16),
-                                                       (32, 8, 2, 1280, 128, "paged", 64)],
+                                                       (32, 8, 2, 1280, 128, "paged", 64),
+                                                       (6, 2, 8, 512, 64, "paged", 32)],
                          ids=["two_heads_per_cta", "one_head_per_cta", "two_heads_d64", "two_heads_paged16",
-                              "two_heads_paged64"])
-def test_prefill_more_items_than_sms(hq, hkv, B, n_q, d, layout, page):
+                              "two_heads_paged64", "one_head_d64_paged32"])
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "all_keys"])
+def test_prefill_more_items_than_sms(hq, hkv, B, n_q, d, layout, page, causal):
     """More 128-row query tiles than SMs: one CTA per SM takes the items from
     the queue, with two heads or one head per CTA; sequences without keys among
-    them, contiguous and paged caches: every output matches the oracle."""
+    them, contiguous and paged caches, causal windows and rows that see every
+    key: every output matches the oracle."""
     spec = small_spec("many_items", B, hq, hkv, d, 1400, layout=layout, page_size=page, seed=33)
     lengths = [0, 800, 650, 700, 720, 0, 790, 800] if B > 2 else [1400, 0]
     case = make_case(spec, "cuda", lengths=lengths)
     q = window_q(case, n_q, seed=14)
-    out, lse = run_prefill(case, q, True)
+    out, lse = run_prefill(case, q, causal)
     torch.cuda.synchronize()
-    ref_out, ref_lse = oracle_rows(case, q, True)
+    ref_out, ref_lse = oracle_rows(case, q, causal)
     assert_close(np64(out), ref_out, "out")
     assert_close(np64(lse), ref_lse, "lse")
 
