@@ -247,3 +247,26 @@ def test_prefill_queue_counters_return_to_zero(hq, hkv):
         assert torch.equal(again[0], first[0]) and torch.equal(again[1], first[1])
     assert torch.all(ws.buf[128:136].cpu() == 0)
     assert fd.workspace_status(ws) == 0
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 2), (3, 3)], ids=["two_heads_per_cta", "one_head_per_cta"])
+@pytest.mark.parametrize("slope", [30.0, 120.0], ids=["rising", "steep"])
+def test_prefill_rising_scores_move_the_max_tile_after_tile(hq, hkv, slope):
+    """Scores that grow along the sequence: each 128-key tile holds keys above
+    the running max, so the softmax keeps taking its max-first path (P made
+    again from the new base) and rescales O tile after tile; the outputs still
+    match the oracle."""
+    T, n_q, D = 1536, 384, 128
+    gen = torch.Generator().manual_seed(41)
+    u = torch.randn(D, generator=gen)
+    u = u / u.norm()
+    ramp = torch.linspace(0.0, 1.0, T)[None, None, :, None]
+    k = (ramp * slope * u + 0.3 * torch.randn(1, hkv, T, D, generator=gen)).to(torch.bfloat16)
+    v = torch.randn(1, hkv, T, D, generator=gen).to(torch.bfloat16)
+    q = 4.0 * u + 0.5 * torch.randn(1, hq, n_q, D, generator=gen)
+    scale = D ** -0.5
+    out, lse = fd.prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, max_seq_len=T, scale=scale)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.decode_rows(np64(q), np64(k), np64(v), scale, causal=True, max_seq_len=T)
+    assert_close(np64(out), ref_out, "out")
+    assert_close(np64(lse), ref_lse, "lse")
