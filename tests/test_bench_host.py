@@ -40,3 +40,21 @@ def test_source_hash_covers_device_files_only():
     assert "fd_api.cu" not in bench.KERNEL_SOURCES + bench.PREFILL_SOURCES
     assert bench.source_hash() != bench.source_hash(bench.PREFILL_SOURCES)
     assert len(bench.source_hash()) == 12
+
+
+def test_committed_summaries_describe_the_current_sources():
+    """Every committed ncu summary names the device-source hash of the kernel it
+    covers, and that hash is the one of the sources as they are now: a kernel
+    edited after its capture shows up here, not as a silently null traffic."""
+    import glob
+    import re
+
+    paths = sorted(glob.glob(os.path.join(bench.ROOT, "profiles", "*.md")))
+    assert paths, "no ncu summaries committed"
+    current = {"split": bench.source_hash(), "prefill": bench.source_hash(bench.PREFILL_SOURCES)}
+    for p in paths:
+        text = open(p).read()
+        m = re.search(r"source_sha:\s*`?([0-9a-f]{12})", text)
+        assert m, f"{os.path.basename(p)} names no source hash"
+        kind = "prefill" if "fd_prefill_kernel" in os.path.basename(p) else "split"
+        assert m.group(1) == current[kind], f"{os.path.basename(p)} was taken on other {kind} sources"
